@@ -1,0 +1,134 @@
+/*
+ * ssd_scan.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD varlen forward
+ * prefill scan.
+ *
+ * The operation is the one defined in the "Per-token recurrence" section of
+ * the Modular page "mamba2_ssd_scan" (Mojo module), for every head h, channel
+ * p and group g = h / (nheads / ngroups):
+ *
+ *     dt_t     = softplus(dt[t,h] + dt_bias[h])     (plain dt + dt_bias when
+ *                                                    dt_softplus == 0)
+ *     dA_t     = exp(A[h] * dt_t)
+ *     state_n  = state_n * dA_t + dt_t * B[t,g,n] * x[t,h,p]
+ *     y[t,h,p] = sum_n C[t,g,n] * state_n + D[h] * x[t,h,p]
+ *
+ * The state starts at zero at every query_start_loc boundary, or at
+ * ssm_pool[cache_indices[b]] when has_initial_state[b] is set, and the state
+ * after the last token of sequence b is written back in place into
+ * ssm_pool[cache_indices[b]] (page "Mamba2SSDChunkScanVarlenFwdInplace",
+ * description and "Tensor shapes").  It is evaluated in the chunked SSD form
+ * described on the kernelindex page "Mamba chunk scan with segsum": chunks of
+ * chunk_size tokens aligned to each sequence start, an intra-chunk diagonal
+ * block, per-chunk states, an inter-chunk state recurrence, and the
+ * off-diagonal contribution.
+ *
+ * Conventions for every entry point:
+ *   - all tensor pointers are DEVICE pointers to contiguous row-major data
+ *     with the shapes listed at ssd_scan_varlen_fwd; the caller owns them;
+ *   - calls are asynchronous on `stream`; no entry point except
+ *     ssd_scan_varlen_read_errors synchronizes;
+ *   - a status other than SSD_OK from a host-side check means that nothing
+ *     was launched and no memory was written.
+ */
+#ifndef SSD_SCAN_H_
+#define SSD_SCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t (NULL = legacy default stream). */
+typedef struct CUstream_st *ssd_stream_t;
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,   /* NULL required pointer, bad size, misaligned pointer */
+    SSD_ERR_UNSUPPORTED = 2,   /* valid but not supported here (head_dim, dstate, chunk_size) */
+    SSD_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than ssd_scan_varlen_workspace_size */
+    SSD_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+    SSD_ERR_DEVICE = 5         /* ssd_scan_varlen_read_errors found a device-side error flag */
+} ssd_status_t;
+
+/* Device-side error flags (bit mask) written into the workspace by a call and
+ * returned by ssd_scan_varlen_read_errors.  Device code never traps: on a bad
+ * index or a wait that runs out it records the flag and skips the work. */
+#define SSD_DEVERR_BAD_QUERY_START_LOC 0x1u /* qsl[0] != 0, decreasing, or qsl[batch] != total_len:
+                                               nothing is computed or written */
+#define SSD_DEVERR_BAD_CACHE_INDEX     0x2u /* cache_indices[b] >= max_slots: that slot access is
+                                               skipped (state read as zero, not written back) */
+#define SSD_DEVERR_TIMEOUT             0x4u /* an on-chip wait (TMA / tensor-core completion)
+                                               exceeded its limit; outputs are incomplete */
+
+/* Largest dstate supported (MAX_DSTATE in the "comptime values" section of
+ * the Modular page "mamba2_ssd_scan"). */
+#define SSD_MAX_DSTATE 256
+
+/* Bytes of device scratch memory that ssd_scan_varlen_fwd needs for these
+ * sizes (chunk table, per-chunk dt / cumulative log-decay, per-chunk states).
+ * Returns 0 when the sizes are invalid or unsupported.  The bound holds for
+ * every query_start_loc with these total_len and batch. */
+SSD_API size_t ssd_scan_varlen_workspace_size(int64_t total_len, int32_t batch, int32_t nheads,
+                                      int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                      int32_t chunk_size);
+
+/* The varlen forward scan with in-place pool write-back.
+ *
+ *   y                 bf16  (total_len, nheads, head_dim)     out: every row written
+ *   x                 bf16  (total_len, nheads, head_dim)
+ *   dt                bf16  (total_len, nheads)
+ *   A                 fp32  (nheads)
+ *   B, C              bf16  (total_len, ngroups, dstate)
+ *   D                 fp32  (nheads)   or NULL (read as 0)
+ *   dt_bias           fp32  (nheads)   or NULL (read as 0)
+ *   ssm_pool          fp32  (max_slots, nheads, head_dim, dstate)  in/out
+ *   query_start_loc   int32 (batch + 1): sequence b is tokens [qsl[b], qsl[b+1])
+ *   has_initial_state uint8 (batch)    or NULL (all false); nonzero = true
+ *   cache_indices     uint32 (batch): pool slot of sequence b; slots must be distinct
+ *   dt_softplus       nonzero: apply softplus to dt + dt_bias
+ *   workspace         device scratch of at least ssd_scan_varlen_workspace_size bytes,
+ *                     256-byte aligned; owned by the caller; contents need no
+ *                     initialisation and are overwritten; one call at a time per workspace
+ *
+ * Only the pool slots named by cache_indices are written (each with the
+ * final state of its sequence, also for a zero-length sequence); every other
+ * pool byte is left unchanged.  Supported: 16 <= head_dim <= 128 and
+ * 16 <= dstate <= 256, both multiples of 16; chunk_size in {64, 128, 256};
+ * nheads % ngroups == 0.  x, B, C, y must be 16-byte aligned.
+ * batch == 0 returns SSD_OK without launching.
+ * Device-data preconditions (qsl monotone from 0 to total_len, slots in
+ * range) are checked on the device; see SSD_DEVERR_*. */
+SSD_API ssd_status_t ssd_scan_varlen_fwd(
+    void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, const float *dt_bias, float *ssm_pool, const int32_t *query_start_loc,
+    const uint8_t *has_initial_state, const uint32_t *cache_indices,
+    int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups,
+    int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+    void *workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* Synchronizes `stream` and returns the device-side error flags (SSD_DEVERR_*)
+ * recorded by the last call that used `workspace`.  Returns SSD_ERR_DEVICE if
+ * any flag is set, SSD_OK otherwise. */
+SSD_API ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stream_t stream,
+                                         uint32_t *flags);
+
+/* A static string naming a status code. */
+SSD_API const char *ssd_status_string(ssd_status_t status);
+
+/* Number of CUDA kernels one ssd_scan_varlen_fwd call launches for these sizes
+ * (0 when batch == 0).  Used to count launches when timing. */
+SSD_API int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_SCAN_H_ */

@@ -1,0 +1,17 @@
+"""GB300-native (sm_103a) Mamba-2 SSD varlen forward prefill scan.
+
+The compute path is the CUDA library libssd_scan.so (C ABI in
+include/ssd_scan.h); ``binding`` is its thin Python front end and
+``workloads`` the seeded synthetic inputs.
+"""
+from .binding import (  # noqa: F401
+    EXPORTED_SYMBOLS,
+    SSDError,
+    alloc_workspace,
+    library,
+    ssd_scan_varlen_fwd,
+    ssd_scan_varlen_num_launches,
+    ssd_scan_varlen_read_errors,
+    ssd_scan_varlen_workspace_size,
+    status_string,
+)

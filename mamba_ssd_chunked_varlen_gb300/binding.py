@@ -1,0 +1,155 @@
+"""Python binding of the C ABI in include/ssd_scan.h (ctypes).
+
+Argument marshalling only: every step of the scan runs in the CUDA kernels of
+libssd_scan.so.  Tensors are torch CUDA tensors (torch provides device memory
+and streams); their shapes give the sizes passed to the C ABI.  There is no
+CPU fallback: if the library is not built, or a tensor is not on a CUDA
+device, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libssd_scan.so")
+
+# Every symbol include/ssd_scan.h declares.
+EXPORTED_SYMBOLS = (
+    "ssd_scan_varlen_workspace_size",
+    "ssd_scan_varlen_fwd",
+    "ssd_scan_varlen_read_errors",
+    "ssd_status_string",
+    "ssd_scan_varlen_num_launches",
+)
+
+SSD_OK = 0
+DEVERR_BAD_QUERY_START_LOC = 0x1
+DEVERR_BAD_CACHE_INDEX = 0x2
+DEVERR_TIMEOUT = 0x4
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class SSDError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+def library() -> ctypes.CDLL:
+    """Load libssd_scan.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "mamba_ssd_chunked_varlen_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.ssd_scan_varlen_workspace_size.restype = sz
+    lib.ssd_scan_varlen_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+    lib.ssd_scan_varlen_fwd.restype = ctypes.c_int
+    lib.ssd_scan_varlen_fwd.argtypes = ([vp] * 12 + [i64, i32, i32, i32, i32, i32, i64, i32, i32]
+                                        + [vp, sz, vp])
+    lib.ssd_scan_varlen_read_errors.restype = ctypes.c_int
+    lib.ssd_scan_varlen_read_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_status_string.argtypes = [ctypes.c_int]
+    lib.ssd_scan_varlen_num_launches.restype = i32
+    lib.ssd_scan_varlen_num_launches.argtypes = [i64, i32]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return library().ssd_status_string(int(status)).decode()
+
+
+def ssd_scan_varlen_workspace_size(total_len: int, batch: int, nheads: int, head_dim: int,
+                                   ngroups: int, dstate: int, chunk_size: int) -> int:
+    return int(library().ssd_scan_varlen_workspace_size(total_len, batch, nheads, head_dim,
+                                                        ngroups, dstate, chunk_size))
+
+
+def ssd_scan_varlen_num_launches(total_len: int, batch: int) -> int:
+    return int(library().ssd_scan_varlen_num_launches(total_len, batch))
+
+
+def _ptr(t, what: str, dtype=None, allow_none: bool = False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{what} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} must have dtype {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() > 0 else ctypes.c_void_p(t.data_ptr() or 0)
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def ssd_scan_varlen_fwd(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
+                        has_initial_state, cache_indices, *, chunk_size: int,
+                        dt_softplus: bool = True, workspace=None, stream=None) -> None:
+    """Run the scan on `stream` (default: torch's current stream).
+
+    Shapes: y, x (T, H, P) bf16; dt (T, H) bf16; A (H,) fp32; B, C (T, G, N)
+    bf16; D, dt_bias (H,) fp32 or None; ssm_pool (slots, H, P, N) fp32 (updated
+    in place); query_start_loc (batch+1,) int32; has_initial_state (batch,)
+    uint8/bool or None; cache_indices (batch,) int32/uint32 (same bits);
+    workspace: a uint8 CUDA tensor of at least ssd_scan_varlen_workspace_size
+    bytes.
+    """
+    import torch
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    batch = query_start_loc.shape[0] - 1
+    if workspace is None:
+        raise ValueError("workspace is required (see ssd_scan_varlen_workspace_size)")
+    if has_initial_state is not None and has_initial_state.dtype == torch.bool:
+        has_initial_state = has_initial_state.view(torch.uint8)
+    if cache_indices.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("cache_indices must be int32 or uint32")
+    st = library().ssd_scan_varlen_fwd(
+        _ptr(y, "y", torch.bfloat16), _ptr(x, "x", torch.bfloat16),
+        _ptr(dt, "dt", torch.bfloat16), _ptr(A, "A", torch.float32),
+        _ptr(B, "B", torch.bfloat16), _ptr(C, "C", torch.bfloat16),
+        _ptr(D, "D", torch.float32, True), _ptr(dt_bias, "dt_bias", torch.float32, True),
+        _ptr(ssm_pool, "ssm_pool", torch.float32), _ptr(query_start_loc, "query_start_loc",
+                                                        torch.int32),
+        _ptr(has_initial_state, "has_initial_state", torch.uint8, True),
+        _ptr(cache_indices, "cache_indices"),
+        T, batch, H, P, G, N, ssm_pool.shape[0], int(chunk_size), int(bool(dt_softplus)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan_varlen_fwd")
+
+
+def ssd_scan_varlen_read_errors(workspace, stream=None) -> int:
+    """Synchronize the stream and return the device-side error flags."""
+    import torch
+    flags = ctypes.c_uint32(0)
+    st = library().ssd_scan_varlen_read_errors(_ptr(workspace, "workspace", torch.uint8),
+                                               _stream_handle(stream), ctypes.byref(flags))
+    if st not in (SSD_OK, 5):
+        raise SSDError(st, "ssd_scan_varlen_read_errors")
+    return int(flags.value)
+
+
+def alloc_workspace(total_len: int, batch: int, nheads: int, head_dim: int, ngroups: int,
+                    dstate: int, chunk_size: int, device="cuda"):
+    """A uint8 torch tensor of the size the C ABI asks for."""
+    import torch
+    n = ssd_scan_varlen_workspace_size(total_len, batch, nheads, head_dim, ngroups, dstate,
+                                       chunk_size)
+    if n == 0:
+        raise SSDError(2, "ssd_scan_varlen_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)

@@ -1,0 +1,226 @@
+// C ABI of the scan (declared in include/ssd_scan.h): argument checks,
+// workspace carving, TMA descriptor encoding and the four stage launches on
+// the caller's stream.  No host synchronisation, no allocation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/ssd_scan.h"
+#include "kernels.cuh"
+
+namespace {
+
+using ssd::ScanParams;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map with a {64, b1, b2} box and 128-byte swizzle.  Elements
+// outside the tensor read as zero.
+bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b1, uint32_t b2)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {64, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Opt-in shared memory per block on sm_100 / sm_103 (227 KB).
+constexpr size_t kMaxSmemPerBlock = 232448;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ssd_status_t check_sizes(int64_t T, int32_t batch, int32_t H, int32_t P, int32_t G, int32_t N,
+                         int32_t Q)
+{
+    if (T < 0 || batch < 0 || H <= 0 || P <= 0 || G <= 0 || N <= 0 || Q <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (H % G != 0)
+        return SSD_ERR_INVALID_ARG;
+    if (N > SSD_MAX_DSTATE)
+        return SSD_ERR_UNSUPPORTED;
+    if (P % 16 != 0 || P > 128 || N % 16 != 0)
+        return SSD_ERR_UNSUPPORTED;
+    if (Q != 64 && Q != 128 && Q != 256)
+        return SSD_ERR_UNSUPPORTED;
+    if (T > INT32_MAX / 2 || static_cast<int64_t>(batch) > INT32_MAX / 2)
+        return SSD_ERR_UNSUPPORTED;
+    ScanParams probe;
+    std::memset(&probe, 0, sizeof probe);
+    probe.P = P;
+    probe.N = N;
+    probe.Q = Q;
+    if (ssd::chunk_state_smem_bytes(probe) > kMaxSmemPerBlock ||
+        ssd::chunk_scan_smem_bytes(probe) > kMaxSmemPerBlock)
+        return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ssd_status_string(ssd_status_t s)
+{
+    switch (s) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_ARG: return "invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "unsupported size";
+    case SSD_ERR_WORKSPACE: return "workspace missing or too small";
+    case SSD_ERR_CUDA: return "CUDA error";
+    case SSD_ERR_DEVICE: return "device-side error flag set";
+    }
+    return "unknown status";
+}
+
+size_t ssd_scan_varlen_workspace_size(int64_t total_len, int32_t batch, int32_t nheads,
+                                      int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                      int32_t chunk_size)
+{
+    if (check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size) != SSD_OK)
+        return 0;
+    return ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, chunk_size).total;
+}
+
+int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
+{
+    if (batch <= 0)
+        return 0;
+    return total_len > 0 ? 4 : 2;
+}
+
+ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const float *A,
+                                 const void *B, const void *C, const float *D,
+                                 const float *dt_bias, float *ssm_pool,
+                                 const int32_t *query_start_loc,
+                                 const uint8_t *has_initial_state, const uint32_t *cache_indices,
+                                 int64_t total_len, int32_t batch, int32_t nheads,
+                                 int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                 int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+                                 void *workspace, size_t workspace_bytes, ssd_stream_t stream_)
+{
+    const ssd_status_t sz =
+        check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size);
+    if (sz != SSD_OK)
+        return sz;
+    if (max_slots < 0)
+        return SSD_ERR_INVALID_ARG;
+    if (batch == 0)
+        return SSD_OK;
+    if (!query_start_loc || !cache_indices || !ssm_pool || !A)
+        return SSD_ERR_INVALID_ARG;
+    if (total_len > 0 && (!y || !x || !dt || !B || !C))
+        return SSD_ERR_INVALID_ARG;
+    if (total_len > 0 && (!aligned16(y) || !aligned16(x) || !aligned16(B) || !aligned16(C)))
+        return SSD_ERR_INVALID_ARG;
+    if (!aligned16(ssm_pool))
+        return SSD_ERR_INVALID_ARG;
+    const ssd::WsLayout L =
+        ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, chunk_size);
+    if (!workspace || workspace_bytes < L.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return SSD_ERR_WORKSPACE;
+    if (L.max_chunks * nheads > INT32_MAX)
+        return SSD_ERR_UNSUPPORTED;
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    ScanParams p;
+    std::memset(&p, 0, sizeof p);
+    p.y = static_cast<__nv_bfloat16 *>(y);
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.dt = static_cast<const __nv_bfloat16 *>(dt);
+    p.A = A;
+    p.D = D;
+    p.dt_bias = dt_bias;
+    p.pool = ssm_pool;
+    p.qsl = query_start_loc;
+    p.has_init = has_initial_state;
+    p.cache_idx = cache_indices;
+    p.T = total_len;
+    p.batch = batch;
+    p.H = nheads;
+    p.P = head_dim;
+    p.G = ngroups;
+    p.N = dstate;
+    p.Q = chunk_size;
+    p.max_slots = max_slots;
+    p.dt_softplus = dt_softplus ? 1 : 0;
+    p.max_chunks = static_cast<int32_t>(L.max_chunks);
+    p.hdr = reinterpret_cast<ssd::WsHeader *>(ws + L.header);
+    p.chunks = reinterpret_cast<ssd::ChunkEntry *>(ws + L.chunks);
+    p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);
+    p.dtp = reinterpret_cast<float *>(ws + L.dtp);
+    p.acum = reinterpret_cast<float *>(ws + L.acum);
+    p.schunk = reinterpret_cast<float *>(ws + L.schunk);
+    p.sprev = reinterpret_cast<__nv_bfloat16 *>(ws + L.sprev);
+
+    ssd::ChunkStateMaps m1;
+    ssd::ChunkScanMaps m3;
+    if (total_len > 0) {
+        const uint64_t T = static_cast<uint64_t>(total_len);
+        const uint64_t H = nheads, P = head_dim, G = ngroups, N = dstate;
+        bool ok = make_map_3d(&m1.B, B, N, G, T, N * 2, G * N * 2, 1, 64) &&
+                  make_map_3d(&m3.B, B, N, G, T, N * 2, G * N * 2, 1, 64) &&
+                  make_map_3d(&m3.C, C, N, G, T, N * 2, G * N * 2, 1, 64) &&
+                  make_map_3d(&m3.X, x, P, H, T, P * 2, H * P * 2, 1, 64) &&
+                  make_map_3d(&m3.Sprev, p.sprev, N, P, static_cast<uint64_t>(L.max_chunks) * H,
+                              N * 2, P * N * 2, 64, 1);
+        if (!ok)
+            return SSD_ERR_CUDA;
+    }
+
+    if (ssd::launch_chunk_table(p, stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (total_len > 0 && ssd::launch_chunk_state(p, m1, stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (ssd::launch_state_passing(p, stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stream_t stream_,
+                                         uint32_t *flags)
+{
+    if (!workspace || !flags)
+        return SSD_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    *flags = v;
+    return v ? SSD_ERR_DEVICE : SSD_OK;
+}
+
+}  // extern "C"

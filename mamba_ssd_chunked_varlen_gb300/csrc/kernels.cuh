@@ -1,0 +1,41 @@
+// Host-side launchers of the four scan stages (one translation unit each).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ssd_common.cuh"
+
+namespace ssd {
+
+// Stage 0: chunk table from query_start_loc, device-side argument checks.
+cudaError_t launch_chunk_table(const ScanParams &p, cudaStream_t stream);
+
+// Stage 1+2c: per (chunk, head) processed dt, cumulative log-decay and the
+// chunk state  S_c[p][n] = sum_j exp(Acum_last - Acum_j) dt_j x[j,p] B[j,n].
+struct ChunkStateMaps {
+    CUtensorMap B;  // bf16 (N, G, T), box {64, 1, 64}, 128-byte swizzle
+};
+size_t chunk_state_smem_bytes(const ScanParams &p);
+cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
+                               cudaStream_t stream);
+
+// Stage 3: inter-chunk state passing; writes the state entering every chunk
+// and the final state of every sequence into its pool slot.
+cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream);
+
+// Stage 2a/2b/4: per (chunk, 128-row tile, head) C.B^T, the masked diagonal
+// block, the off-diagonal C.S_prev^T term and the D skip; writes y.
+struct ChunkScanMaps {
+    CUtensorMap C;      // bf16 (N, G, T), box {64, 1, 64}
+    CUtensorMap B;      // bf16 (N, G, T), box {64, 1, 64}
+    CUtensorMap X;      // bf16 (P, H, T), box {64, 1, 64}
+    CUtensorMap Sprev;  // bf16 (N, P, chunks*H), box {64, 64, 1}
+};
+size_t chunk_scan_smem_bytes(const ScanParams &p);
+cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps,
+                              cudaStream_t stream);
+
+inline int pad64(int v) { return (v + 63) / 64 * 64; }
+
+}  // namespace ssd

@@ -1,0 +1,93 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/ssd_scan.h declares, sizes its workspace, and rejects bad
+arguments before touching the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mamba_ssd_chunked_varlen_gb300 import binding
+from mamba_ssd_chunked_varlen_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return binding.library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssd_scan.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(binding.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "ok"
+    assert "workspace" in binding.status_string(3)
+
+
+def test_workspace_size(lib):
+    ws = binding.ssd_scan_varlen_workspace_size
+    n1 = ws(4096, 1, 16, 64, 1, 256, 256)
+    # chunk states dominate: (ceil(T/Q) + batch) chunks x H x P x N x (4 + 2) bytes
+    assert n1 >= 17 * 16 * 64 * 256 * 6
+    assert n1 < 17 * 16 * 64 * 256 * 6 + 17 * 16 * 256 * 8 + 64 * 1024
+    assert ws(4096, 2, 16, 64, 1, 256, 256) > n1          # more sequences, more chunks
+    assert ws(0, 3, 4, 32, 1, 32, 64) > 0                 # empty sequences still need a table
+    assert ws(512, 1, 4, 32, 1, 512, 64) == 0             # dstate > 256 (MAX_DSTATE)
+    assert ws(512, 1, 4, 32, 1, 32, 100) == 0             # unsupported chunk size
+    assert ws(512, 1, 6, 32, 4, 32, 64) == 0              # nheads % ngroups != 0
+    assert ws(512, 1, 4, 24, 1, 32, 64) == 0              # head_dim not a multiple of 16
+    assert ws(512, 1, 4, 256, 1, 32, 64) == 0             # head_dim > 128
+
+
+def test_launch_count(lib):
+    assert binding.ssd_scan_varlen_num_launches(4096, 1) == 4
+    assert binding.ssd_scan_varlen_num_launches(0, 3) == 2
+    assert binding.ssd_scan_varlen_num_launches(10, 0) == 0
+
+
+def _call(lib, **over):
+    args = dict(y=1 << 12, x=1 << 12, dt=1 << 12, A=1 << 12, B=1 << 12, C=1 << 12, D=None,
+                dt_bias=None, pool=1 << 12, qsl=1 << 12, hinit=None, cidx=1 << 12,
+                T=512, batch=1, H=4, P=32, G=1, N=32, slots=4, Q=64, sp=1,
+                ws=1 << 12, wsb=1 << 30)
+    args.update(over)
+    vp = lambda v: None if v is None else ctypes.c_void_p(v)
+    return lib.ssd_scan_varlen_fwd(
+        vp(args["y"]), vp(args["x"]), vp(args["dt"]), vp(args["A"]), vp(args["B"]),
+        vp(args["C"]), vp(args["D"]), vp(args["dt_bias"]), vp(args["pool"]), vp(args["qsl"]),
+        vp(args["hinit"]), vp(args["cidx"]), args["T"], args["batch"], args["H"], args["P"],
+        args["G"], args["N"], args["slots"], args["Q"], args["sp"], vp(args["ws"]),
+        args["wsb"], None)
+
+
+def test_host_checks_reject_before_any_launch(lib):
+    # None of these reach the GPU: every one fails a host-side check first.
+    assert _call(lib, x=None) == 1                 # NULL required pointer
+    assert _call(lib, qsl=None) == 1
+    assert _call(lib, G=3) == 1                    # nheads % ngroups
+    assert _call(lib, N=512) == 2                  # dstate > MAX_DSTATE
+    assert _call(lib, Q=32) == 2                   # chunk size
+    assert _call(lib, P=24) == 2                   # head_dim
+    assert _call(lib, x=(1 << 12) + 2) == 1        # misaligned (TMA needs 16 B)
+    assert _call(lib, ws=None) == 3                # workspace
+    assert _call(lib, wsb=16) == 3
+    assert _call(lib, ws=(1 << 12) + 16) == 3      # workspace alignment
+    assert _call(lib, T=-1) == 1
+    assert _call(lib, batch=0, x=None, y=None) == 0  # empty batch: nothing to do
