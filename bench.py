@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Benchmark of the Mamba-2 SSD varlen forward prefill scan on GB300.
+
+One step = one ssd_scan_varlen_fwd call (all four stages: chunk table, chunk
+state, state passing, chunk scan) on the kernelindex-shaped workload: one
+4096-token sequence, nheads=16, head_dim=64, ngroups=1, dstate=256, chunk 256
+(the head/state shape of the kernelindex "Mamba chunk scan with segsum"
+suite, whose cases are not published).  Inputs are seeded synthetic data
+resident in HBM; the L2 cache is flushed (a 512 MB write) before every timed
+call, because this workload's 22 MB of inputs would otherwise stay in the
+129 MB L2.
+
+Prints ONE JSON line on rank 0:
+  value       tokens/s over all ranks (replicas: every rank runs the same
+              independent workload; weak scaling), from CUDA events around
+              each call on the launching stream
+  e2e         the same metric through the public API with host buffers: the
+              pinned-host -> device copies of the step's inputs, the call and
+              the device -> host copy of y inside the timed region
+  roofline    the dominant kernel's achieved bytes (or flops) per launch over
+              its event-timed duration, against the measured peak
+  cpu_baseline  the fp64 oracle on this machine's host cores (a bounded sample)
+
+`--impl reference` times the oracle instead (the reference arm), on the same
+workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mamba_ssd_chunked_varlen_gb300 import workloads as W  # noqa: E402
+
+METRIC = "SSD scan tokens/s and µs/call on 1 GB300; % of tensor/HBM roofline"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+STAGES = ("chunk_table", "chunk_state", "state_passing", "chunk_scan")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(want_gpus: int):
+    """Returns (rank, world, local_rank); initialises NCCL when launched by torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("SSD_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def dist_reduce(value: float, op: str) -> float:
+    """max / sum of a float over ranks (identity on one process)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- work model
+
+def chunk_lengths(w) -> list:
+    out = []
+    for L in w.seq_lens:
+        L = int(L)
+        for s in range(0, L, w.chunk_size):
+            out.append((min(w.chunk_size, L - s), s == 0))
+    return out
+
+
+def work_model(w) -> dict:
+    """Algorithmic bytes and flops per call and per stage.
+
+    Bytes are compulsory I/O only: x, dt, B, C read once, y written once,
+    pool slots read (with an initial state) and written.  Flops are the
+    chunked SSD form with exact causal triangles: C.B^T once per group,
+    the diagonal block per head, the chunk state per head, the off-diagonal
+    term per head (skipped for a first chunk without initial state).
+    """
+    T, H, P, G, N = w.total_len, w.nheads, w.head_dim, w.ngroups, w.dstate
+    hinit = (np.zeros(w.batch, bool) if w.has_initial_state is None
+             else w.has_initial_state.astype(bool))
+    x_b = T * H * P * 2
+    y_b = T * H * P * 2
+    dt_b = T * H * 2
+    bc_b = T * G * N * 2
+    slot_b = H * P * N * 4
+    pool_r = int(hinit.sum()) * slot_b
+    pool_w = w.batch * slot_b
+    f_cb = f_diag = f_state = f_off = 0
+    seq_of_chunk = []
+    for b, L in enumerate(w.seq_lens):
+        for s in range(0, int(L), w.chunk_size):
+            seq_of_chunk.append((b, min(w.chunk_size, int(L) - s), s == 0))
+    for b, l, first in seq_of_chunk:
+        tri = l * (l + 1) // 2
+        f_cb += G * tri * N * 2
+        f_diag += H * tri * P * 2
+        f_state += H * l * N * P * 2
+        if not (first and not hinit[b]):
+            f_off += H * l * N * P * 2
+    stages = {
+        "chunk_table": {"bytes": (w.batch + 1) * 4 + w.batch * 4, "flops": 0},
+        "chunk_state": {"bytes": x_b + bc_b + dt_b, "flops": f_state},
+        "state_passing": {"bytes": pool_r + pool_w, "flops": 0},
+        "chunk_scan": {"bytes": x_b + 2 * bc_b + dt_b + y_b, "flops": f_cb + f_diag + f_off},
+    }
+    return {
+        "bytes": x_b + dt_b + 2 * bc_b + y_b + pool_r + pool_w,
+        "flops": f_cb + f_diag + f_state + f_off,
+        "stages": stages,
+        "chunks": len(seq_of_chunk),
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        d = dict(FALLBACK_PEAKS)
+        d["source"] = "fallback"
+        return d
+
+
+def kernel_source_hash(stage: str) -> str:
+    path = os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc", f"{stage}.cu")
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc", "sm100_ptx.cuh"),
+              os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc", "ssd_common.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(stage: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary table
+    (profiles/dram_traffic.md), if it was taken on the current source of that
+    kernel; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == workload and cells[1] == stage:
+            if cells[2] != kernel_source_hash(stage):
+                return None
+            try:
+                return int(cells[3])
+            except ValueError:
+                return None
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = None
+        self.dev = device_index
+
+    def start(self):
+        import torch
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
+        except Exception:
+            uuid = str(self.dev)
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            text = ""
+        rows = []
+        for line in text.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[4 + i].lower().startswith("active")})
+        pw = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, local):
+    import torch
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    from mamba_ssd_chunked_varlen_gb300 import build as cuda_build
+
+    if not os.path.exists(os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "libssd_scan.so")):
+        cuda_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    w = W.workload(args.workload)
+    model = work_model(w)
+    T = w.total_len
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    d = dict(x=bf(w.x), dt=bf(w.dt), A=torch.from_numpy(w.A).to(dev), B=bf(w.B), C=bf(w.C),
+             D=torch.from_numpy(w.D).to(dev), dt_bias=torch.from_numpy(w.dt_bias).to(dev),
+             pool=torch.from_numpy(w.ssm_pool).to(dev),
+             qsl=torch.from_numpy(w.query_start_loc).to(dev),
+             hinit=torch.from_numpy(w.has_initial_state).to(dev),
+             cidx=torch.from_numpy(w.cache_indices.astype(np.int32)).to(dev))
+    y = torch.empty(w.x.shape, dtype=torch.bfloat16, device=dev)
+    ws = pkg.alloc_workspace(T, w.batch, w.nheads, w.head_dim, w.ngroups, w.dstate,
+                             w.chunk_size, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def call(yy=None, dd=None):
+        dd = d if dd is None else dd
+        pkg.ssd_scan_varlen_fwd(yy if yy is not None else y, dd["x"], dd["dt"], d["A"], dd["B"],
+                                dd["C"], d["D"], d["dt_bias"], d["pool"], dd["qsl"],
+                                dd["hinit"], dd["cidx"], chunk_size=w.chunk_size,
+                                dt_softplus=w.dt_softplus, workspace=ws, stream=stream)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    flags = pkg.ssd_scan_varlen_read_errors(ws, stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x}")
+
+    # ---- timed region: K calls, L2 flushed before each, events around each call
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.1)
+    dist_barrier()
+    torch.cuda.synchronize(dev)
+    for k in range(K):
+        flush.fill_(k)
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier()
+    clocks = sampler.stop()
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = sum(times_ms) / K
+    mean_ms_all = dist_reduce(mean_ms, "max")
+    tokens_all = T * world
+    value = tokens_all / (mean_ms_all * 1e-3)
+
+    # ---- per-stage attribution (stage events between the four launches)
+    Kp = min(K, 500)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(Kp)]
+    for k in range(Kp):
+        flush.fill_(k)
+        pkg.ssd_scan_varlen_fwd_profiled(
+            y, d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], d["pool"], d["qsl"],
+            d["hinit"], d["cidx"], chunk_size=w.chunk_size, dt_softplus=w.dt_softplus,
+            workspace=ws, stream=stream, events=sev[k])
+    torch.cuda.synchronize(dev)
+    stage_ms = {s: sum(sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(Kp)) / Kp
+                for i, s in enumerate(STAGES)}
+
+    # ---- end to end through the public API with host buffers
+    Ke = min(K, 500)
+    host_np = {"x": w.x.view(np.int16), "dt": w.dt.view(np.int16), "B": w.B.view(np.int16),
+               "C": w.C.view(np.int16), "qsl": w.query_start_loc,
+               "hinit": w.has_initial_state, "cidx": w.cache_indices.astype(np.int32)}
+    host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host_np.items()}
+    dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host.items()}
+    y_host = torch.empty(w.x.shape, dtype=torch.int16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = y_host.numel() * 2
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Ke)]
+    for k in range(Ke):
+        flush.fill_(k)
+        eev[k][0].record(stream)
+        for key, hv in host.items():
+            dev_in[key].copy_(hv, non_blocking=True)
+        dd = {key: (dev_in[key].view(torch.bfloat16) if key in ("x", "dt", "B", "C") else
+                    dev_in[key]) for key in dev_in}
+        call(dd=dd)
+        y_host.copy_(y.view(torch.int16), non_blocking=True)
+        eev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / Ke
+    e2e_ms_all = dist_reduce(e2e_ms, "max")
+    flags = pkg.ssd_scan_varlen_read_errors(ws, stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x}")
+
+    # ---- roofline of the dominant kernel
+    peaks = load_peaks()
+    dom = max(STAGES, key=lambda s: stage_ms[s])
+    st = model["stages"][dom]
+    t_s = stage_ms[dom] * 1e-3
+    t_bytes = st["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_flops = st["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_flops > t_bytes:
+        achieved = st["flops"] / t_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    else:
+        achieved = st["bytes"] / t_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    roof["traffic"] = measured_traffic(dom, args.workload)
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"] + " (burst)"
+    roof["algorithmic_bytes"] = st["bytes"]
+    roof["algorithmic_flops"] = st["flops"]
+    roof["us_per_launch"] = round(stage_ms[dom] * 1e3, 3)
+    t_roof = max(model["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                 model["flops"] / (peaks["bf16_tflops"] * 1e12))
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(mean_ms_all, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and value recipe of the workload)",
+        "config": {"workload": w.name, "total_len": T, "batch": w.batch, "nheads": w.nheads,
+                   "head_dim": w.head_dim, "ngroups": w.ngroups, "dstate": w.dstate,
+                   "chunk_size": w.chunk_size, "chunks": model["chunks"],
+                   "l2": f"flushed before every timed call ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": round(mean_ms_all * 1e3, 3),
+        "us_per_call_median": round(statistics.median(times_ms) * 1e3, 3),
+        "roofline": roof,
+        "roofline_call": {"t_roofline_us": round(t_roof * 1e6, 3),
+                          "frac": round(t_roof / (mean_ms_all * 1e-3), 4),
+                          "bytes": model["bytes"], "flops": model["flops"]},
+        "stages_us": {s: round(stage_ms[s] * 1e3, 3) for s in STAGES},
+        "e2e": {"value": round(tokens_all / (e2e_ms_all * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(e2e_ms_all * 1e3, 3)},
+        "gpu_launches": K * pkg.ssd_scan_varlen_num_launches(T, w.batch),
+        "clocks": clocks,
+    }
+    return result, w
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_time(w, budget_s: float, min_reps: int = 1, max_reps: int = 50):
+    """Median seconds per oracle call on a sample of `w` (sampling heads when a
+    full call would exceed the budget).  Returns (value tokens/s, info)."""
+    from oracle import recurrence
+    t0 = time.perf_counter()
+    recurrence.run_workload(w)
+    t_full = time.perf_counter() - t0
+    heads = w.nheads
+    if t_full > budget_s:
+        heads = max(1, int(w.nheads * budget_s / t_full))
+    times = []
+    start = time.perf_counter()
+    while len(times) < max_reps:
+        t0 = time.perf_counter()
+        recurrence.run_workload(w, heads=(0, heads))
+        times.append(time.perf_counter() - t0)
+        if len(times) >= min_reps and time.perf_counter() - start >= budget_s:
+            break
+    med = statistics.median(times)
+    value = w.total_len * (heads / w.nheads) / med
+    cores = min(recurrence.max_threads(), w.batch * heads)
+    sample = (f"{w.name}: {w.total_len} tokens x {heads}/{w.nheads} heads per call, "
+              f"{len(times)} calls, median {med * 1e3:.1f} ms")
+    return value, cores, sample, med, heads
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = W.workload(args.workload)
+    from oracle import build as oracle_build
+    oracle_build.build()
+    from oracle import recurrence
+    # size each step so that warmup + steps finish in about two minutes
+    t0 = time.perf_counter()
+    recurrence.run_workload(w)
+    t_full = time.perf_counter() - t0
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    heads = w.nheads if t_full <= per_step else max(1, int(w.nheads * per_step / t_full))
+    for _ in range(args.warmup):
+        recurrence.run_workload(w, heads=(0, heads))
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        recurrence.run_workload(w, heads=(0, heads))
+        times.append(time.perf_counter() - t0)
+    mean = sum(times) / len(times)
+    value = w.total_len * (heads / w.nheads) / mean
+    cores = min(recurrence.max_threads(), w.batch * heads)
+    sample = (f"{w.name}: {w.total_len} tokens x {heads}/{w.nheads} heads per step "
+              f"(tokens/s scaled by the head fraction)")
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes and value recipe of the workload)",
+        "config": {"workload": w.name, "total_len": w.total_len, "batch": w.batch,
+                   "nheads": w.nheads, "head_dim": w.head_dim, "ngroups": w.ngroups,
+                   "dstate": w.dstate, "chunk_size": w.chunk_size,
+                   "parallelism": "host cores (OpenMP over sequence x head)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="kernelindex", choices=W.WORKLOADS)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    rank, world, local = dist_setup(args.gpus)
+    result, w = run_ours(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            value, cores, sample, _, _ = oracle_time(w, args.cpu_budget)
+            result["cpu_baseline"] = {"value": round(value, 1), "unit": UNIT, "cores": cores,
+                                      "kind": "oracle", "sample": sample}
+        else:
+            result["cpu_baseline"] = None
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

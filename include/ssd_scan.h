@@ -114,6 +114,21 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd(
     int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
     void *workspace, size_t workspace_bytes, ssd_stream_t stream);
 
+/* ssd_scan_varlen_fwd with per-stage timing: `events` points to 5 CUDA events
+ * (cudaEvent_t, created by the caller) that are recorded on `stream` before
+ * stage 0 and after each of the four stages (chunk table, chunk state, state
+ * passing, chunk scan); cudaEventElapsedTime between consecutive events gives
+ * each stage's device time.  Otherwise identical to ssd_scan_varlen_fwd
+ * (same arguments, results and errors).  The extra records put a small gap
+ * between stages, so use it to attribute time, not to time the whole call. */
+SSD_API ssd_status_t ssd_scan_varlen_fwd_profiled(
+    void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, const float *dt_bias, float *ssm_pool, const int32_t *query_start_loc,
+    const uint8_t *has_initial_state, const uint32_t *cache_indices,
+    int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups,
+    int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+    void *workspace, size_t workspace_bytes, ssd_stream_t stream, void *const *events);
+
 /* Synchronizes `stream` and returns the device-side error flags (SSD_DEVERR_*)
  * recorded by the last call that used `workspace`.  Returns SSD_ERR_DEVICE if
  * any flag is set, SSD_OK otherwise. */

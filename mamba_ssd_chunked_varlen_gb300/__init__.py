@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     alloc_workspace,
     library,
     ssd_scan_varlen_fwd,
+    ssd_scan_varlen_fwd_profiled,
     ssd_scan_varlen_num_launches,
     ssd_scan_varlen_read_errors,
     ssd_scan_varlen_workspace_size,

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libssd_scan
 EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_workspace_size",
     "ssd_scan_varlen_fwd",
+    "ssd_scan_varlen_fwd_profiled",
     "ssd_scan_varlen_read_errors",
     "ssd_status_string",
     "ssd_scan_varlen_num_launches",
@@ -52,6 +53,8 @@ def library() -> ctypes.CDLL:
     lib.ssd_scan_varlen_fwd.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd.argtypes = ([vp] * 12 + [i64, i32, i32, i32, i32, i32, i64, i32, i32]
                                         + [vp, sz, vp])
+    lib.ssd_scan_varlen_fwd_profiled.restype = ctypes.c_int
+    lib.ssd_scan_varlen_fwd_profiled.argtypes = lib.ssd_scan_varlen_fwd.argtypes + [vp]
     lib.ssd_scan_varlen_read_errors.restype = ctypes.c_int
     lib.ssd_scan_varlen_read_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ssd_status_string.restype = ctypes.c_char_p
@@ -96,6 +99,51 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+              cache_indices, chunk_size, dt_softplus, workspace, stream):
+    import torch
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    batch = query_start_loc.shape[0] - 1
+    if workspace is None:
+        raise ValueError("workspace is required (see ssd_scan_varlen_workspace_size)")
+    if has_initial_state is not None and has_initial_state.dtype == torch.bool:
+        has_initial_state = has_initial_state.view(torch.uint8)
+    if cache_indices.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("cache_indices must be int32 or uint32")
+    return (
+        _ptr(y, "y", torch.bfloat16), _ptr(x, "x", torch.bfloat16),
+        _ptr(dt, "dt", torch.bfloat16), _ptr(A, "A", torch.float32),
+        _ptr(B, "B", torch.bfloat16), _ptr(C, "C", torch.bfloat16),
+        _ptr(D, "D", torch.float32, True), _ptr(dt_bias, "dt_bias", torch.float32, True),
+        _ptr(ssm_pool, "ssm_pool", torch.float32), _ptr(query_start_loc, "query_start_loc",
+                                                        torch.int32),
+        _ptr(has_initial_state, "has_initial_state", torch.uint8, True),
+        _ptr(cache_indices, "cache_indices"),
+        T, batch, H, P, G, N, ssm_pool.shape[0], int(chunk_size), int(bool(dt_softplus)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
+
+
+def ssd_scan_varlen_fwd_profiled(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
+                                 has_initial_state, cache_indices, *, chunk_size: int,
+                                 dt_softplus: bool = True, workspace=None, stream=None,
+                                 events=None) -> None:
+    """ssd_scan_varlen_fwd that also records 5 torch.cuda.Event objects around
+    the four stages (chunk table, chunk state, state passing, chunk scan)."""
+    if events is None or len(events) != 5:
+        raise ValueError("events must be 5 torch.cuda.Event objects")
+    import torch
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event lazily, on first record
+            e.record(torch.cuda.current_stream() if stream is None else stream)
+    handles = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    st = library().ssd_scan_varlen_fwd_profiled(
+        *_fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+                   cache_indices, chunk_size, dt_softplus, workspace, stream), handles)
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan_varlen_fwd_profiled")
+
+
 def ssd_scan_varlen_fwd(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
                         has_initial_state, cache_indices, *, chunk_size: int,
                         dt_softplus: bool = True, workspace=None, stream=None) -> None:
@@ -108,27 +156,9 @@ def ssd_scan_varlen_fwd(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc
     workspace: a uint8 CUDA tensor of at least ssd_scan_varlen_workspace_size
     bytes.
     """
-    import torch
-    T, H, P = x.shape
-    G, N = B.shape[1], B.shape[2]
-    batch = query_start_loc.shape[0] - 1
-    if workspace is None:
-        raise ValueError("workspace is required (see ssd_scan_varlen_workspace_size)")
-    if has_initial_state is not None and has_initial_state.dtype == torch.bool:
-        has_initial_state = has_initial_state.view(torch.uint8)
-    if cache_indices.dtype not in (torch.int32, torch.uint32):
-        raise ValueError("cache_indices must be int32 or uint32")
     st = library().ssd_scan_varlen_fwd(
-        _ptr(y, "y", torch.bfloat16), _ptr(x, "x", torch.bfloat16),
-        _ptr(dt, "dt", torch.bfloat16), _ptr(A, "A", torch.float32),
-        _ptr(B, "B", torch.bfloat16), _ptr(C, "C", torch.bfloat16),
-        _ptr(D, "D", torch.float32, True), _ptr(dt_bias, "dt_bias", torch.float32, True),
-        _ptr(ssm_pool, "ssm_pool", torch.float32), _ptr(query_start_loc, "query_start_loc",
-                                                        torch.int32),
-        _ptr(has_initial_state, "has_initial_state", torch.uint8, True),
-        _ptr(cache_indices, "cache_indices"),
-        T, batch, H, P, G, N, ssm_pool.shape[0], int(chunk_size), int(bool(dt_softplus)),
-        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
+        *_fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+                   cache_indices, chunk_size, dt_softplus, workspace, stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_scan_varlen_fwd")
 

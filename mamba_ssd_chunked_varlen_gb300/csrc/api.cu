@@ -52,9 +52,6 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Opt-in shared memory per block on sm_100 / sm_103 (227 KB).
-constexpr size_t kMaxSmemPerBlock = 232448;
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 ssd_status_t check_sizes(int64_t T, int32_t batch, int32_t H, int32_t P, int32_t G, int32_t N,
@@ -77,8 +74,8 @@ ssd_status_t check_sizes(int64_t T, int32_t batch, int32_t H, int32_t P, int32_t
     probe.P = P;
     probe.N = N;
     probe.Q = Q;
-    if (ssd::chunk_state_smem_bytes(probe) > kMaxSmemPerBlock ||
-        ssd::chunk_scan_smem_bytes(probe) > kMaxSmemPerBlock)
+    if (ssd::chunk_state_smem_bytes(probe) > static_cast<size_t>(ssd::kMaxSmemPerBlock) ||
+        ssd::chunk_scan_smem_bytes(probe) > static_cast<size_t>(ssd::kMaxSmemPerBlock))
         return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
 }
@@ -116,15 +113,18 @@ int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
     return total_len > 0 ? 4 : 2;
 }
 
-ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const float *A,
-                                 const void *B, const void *C, const float *D,
-                                 const float *dt_bias, float *ssm_pool,
-                                 const int32_t *query_start_loc,
-                                 const uint8_t *has_initial_state, const uint32_t *cache_indices,
-                                 int64_t total_len, int32_t batch, int32_t nheads,
-                                 int32_t head_dim, int32_t ngroups, int32_t dstate,
-                                 int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
-                                 void *workspace, size_t workspace_bytes, ssd_stream_t stream_)
+}  // extern "C"
+
+namespace {
+
+ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
+                       const void *C, const float *D, const float *dt_bias, float *ssm_pool,
+                       const int32_t *query_start_loc, const uint8_t *has_initial_state,
+                       const uint32_t *cache_indices, int64_t total_len, int32_t batch,
+                       int32_t nheads, int32_t head_dim, int32_t ngroups, int32_t dstate,
+                       int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+                       void *workspace, size_t workspace_bytes, ssd_stream_t stream_,
+                       void *const *events)
 {
     const ssd_status_t sz =
         check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size);
@@ -197,15 +197,58 @@ ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const f
             return SSD_ERR_CUDA;
     }
 
-    if (ssd::launch_chunk_table(p, stream) != cudaSuccess)
+    auto mark = [&](int k) {
+        return events == nullptr ||
+               cudaEventRecord(static_cast<cudaEvent_t>(events[k]), stream) == cudaSuccess;
+    };
+    if (!mark(0) || ssd::launch_chunk_table(p, stream) != cudaSuccess || !mark(1))
         return SSD_ERR_CUDA;
     if (total_len > 0 && ssd::launch_chunk_state(p, m1, stream) != cudaSuccess)
         return SSD_ERR_CUDA;
-    if (ssd::launch_state_passing(p, stream) != cudaSuccess)
+    if (!mark(2) || ssd::launch_state_passing(p, stream) != cudaSuccess || !mark(3))
         return SSD_ERR_CUDA;
     if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream) != cudaSuccess)
         return SSD_ERR_CUDA;
+    if (!mark(4))
+        return SSD_ERR_CUDA;
     return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const float *A,
+                                 const void *B, const void *C, const float *D,
+                                 const float *dt_bias, float *ssm_pool,
+                                 const int32_t *query_start_loc,
+                                 const uint8_t *has_initial_state, const uint32_t *cache_indices,
+                                 int64_t total_len, int32_t batch, int32_t nheads,
+                                 int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                 int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+                                 void *workspace, size_t workspace_bytes, ssd_stream_t stream)
+{
+    return scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+                     cache_indices, total_len, batch, nheads, head_dim, ngroups, dstate, max_slots,
+                     chunk_size, dt_softplus, workspace, workspace_bytes, stream, nullptr);
+}
+
+ssd_status_t ssd_scan_varlen_fwd_profiled(
+    void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, const float *dt_bias, float *ssm_pool, const int32_t *query_start_loc,
+    const uint8_t *has_initial_state, const uint32_t *cache_indices, int64_t total_len,
+    int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups, int32_t dstate,
+    int64_t max_slots, int32_t chunk_size, int32_t dt_softplus, void *workspace,
+    size_t workspace_bytes, ssd_stream_t stream, void *const *events)
+{
+    if (!events)
+        return SSD_ERR_INVALID_ARG;
+    for (int k = 0; k < 5; ++k)
+        if (!events[k])
+            return SSD_ERR_INVALID_ARG;
+    return scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+                     cache_indices, total_len, batch, nheads, head_dim, ngroups, dstate, max_slots,
+                     chunk_size, dt_softplus, workspace, workspace_bytes, stream, events);
 }
 
 ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stream_t stream_,

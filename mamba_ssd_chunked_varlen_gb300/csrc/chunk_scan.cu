@@ -277,6 +277,8 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+SmemOptIn s_smem_configured;
+
 }  // namespace
 
 size_t chunk_scan_smem_bytes(const ScanParams &p)
@@ -290,9 +292,7 @@ cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps,
     const int P_pad = pad64(p.P), N_pad = pad64(p.N);
     const int n_itiles = (p.Q + 127) / 128;
     const size_t smem = chunk_scan_smem_bytes(p);
-    cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void *>(chunk_scan_kernel), s_smem_configured);
     if (e != cudaSuccess)
         return e;
     dim3 grid(p.max_chunks * n_itiles, p.H);

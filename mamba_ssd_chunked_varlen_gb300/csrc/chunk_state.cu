@@ -266,6 +266,8 @@ inline uint32_t pow2_cols(uint32_t v)
     return c;
 }
 
+SmemOptIn s_smem_configured;
+
 }  // namespace
 
 size_t chunk_state_smem_bytes(const ScanParams &p)
@@ -280,9 +282,7 @@ cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
     const int n_mtiles = mtiles_of(p.N);
     const uint32_t cols = pow2_cols(static_cast<uint32_t>(n_mtiles * P_pad));
     const size_t smem = chunk_state_smem_bytes(p);
-    cudaError_t e = cudaFuncSetAttribute(chunk_state_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void *>(chunk_state_kernel), s_smem_configured);
     if (e != cudaSuccess)
         return e;
     dim3 grid(p.max_chunks, p.H);

@@ -1,6 +1,9 @@
 // Host-side launchers of the four scan stages (one translation unit each).
 #pragma once
 
+#include <atomic>
+#include <cstdint>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -37,5 +40,28 @@ cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps,
                               cudaStream_t stream);
 
 inline int pad64(int v) { return (v + 63) / 64 * 64; }
+
+// Opt-in shared memory per block on sm_100 / sm_103 (227 KB).
+constexpr int kMaxSmemPerBlock = 232448;
+
+// Per-device record of whether a kernel's dynamic shared-memory limit has been
+// raised to kMaxSmemPerBlock (done once per device and kernel, not per call).
+struct SmemOptIn {
+    std::atomic<uint8_t> done[64];
+};
+
+inline cudaError_t ensure_max_smem(const void *kernel, SmemOptIn &state)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && state.done[dev].load(std::memory_order_acquire))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerBlock);
+    if (e == cudaSuccess && dev >= 0 && dev < 64)
+        state.done[dev].store(1, std::memory_order_release);
+    return e;
+}
 
 }  // namespace ssd
