@@ -55,7 +55,9 @@ typedef enum {
     SSD_ERR_UNSUPPORTED = 2,   /* valid but not supported here (head_dim, dstate, chunk_size) */
     SSD_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than ssd_scan_varlen_workspace_size */
     SSD_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
-    SSD_ERR_DEVICE = 5         /* ssd_scan_varlen_read_errors found a device-side error flag */
+    SSD_ERR_DEVICE = 5,        /* ssd_scan_varlen_read_errors found a device-side error flag */
+    SSD_ERR_TOO_LARGE = 6      /* ssd_scan_varlen_fwd_noalloc: the sizes need more scratch than
+                                  its built-in buffer (SSD_NOALLOC_SCRATCH_BYTES) */
 } ssd_status_t;
 
 /* Device-side error flags (bit mask) written into the workspace by a call and
@@ -128,6 +130,40 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd_profiled(
     int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups,
     int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
     void *workspace, size_t workspace_bytes, ssd_stream_t stream, void *const *events);
+
+/* Size of the scratch buffer built into the library for
+ * ssd_scan_varlen_fwd_noalloc (32 MiB of device memory on every GPU that
+ * loads the library, held until the process exits). */
+#define SSD_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* The scan for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this entry point; it exists for host code that may not
+ * call cudaMalloc or any allocating library routine, such as a plugin inside
+ * a host framework that owns all device memory and hands out no allocator,
+ * or a serving loop that forbids allocation once it is running.
+ *
+ * Same arguments, results and errors as ssd_scan_varlen_fwd, minus the
+ * workspace: the scratch lives in a fixed SSD_NOALLOC_SCRATCH_BYTES device
+ * array inside the library.  Sizes whose ssd_scan_varlen_workspace_size
+ * exceeds it return SSD_ERR_TOO_LARGE without launching (32 MiB fits, for
+ * example, one 4096-token sequence with nheads 16, head_dim 64, dstate 256,
+ * chunk 256).  The caller still passes every input and output.
+ *
+ * The first call on each device looks up that device's address of the array
+ * (with the device current); make that first call before any stream capture.
+ * It allocates nothing, now or later.  All calls on a device share the one
+ * array and it keeps the last call's contents (each call rewrites everything
+ * it reads, so nothing needs clearing); calls whose execution overlaps on the
+ * GPU (different streams, or different host threads) race on it and must be
+ * serialised by the caller.  Device-side error flags (SSD_DEVERR_*) of these
+ * calls stay in the built-in array and are not reported. */
+SSD_API ssd_status_t ssd_scan_varlen_fwd_noalloc(
+    void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, const float *dt_bias, float *ssm_pool, const int32_t *query_start_loc,
+    const uint8_t *has_initial_state, const uint32_t *cache_indices,
+    int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups,
+    int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+    ssd_stream_t stream);
 
 /* Synchronizes `stream` and returns the device-side error flags (SSD_DEVERR_*)
  * recorded by the last call that used `workspace`.  Returns SSD_ERR_DEVICE if

@@ -19,12 +19,15 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_workspace_size",
     "ssd_scan_varlen_fwd",
     "ssd_scan_varlen_fwd_profiled",
+    "ssd_scan_varlen_fwd_noalloc",
     "ssd_scan_varlen_read_errors",
     "ssd_status_string",
     "ssd_scan_varlen_num_launches",
 )
 
 SSD_OK = 0
+SSD_ERR_TOO_LARGE = 6
+NOALLOC_SCRATCH_BYTES = 32 << 20  # SSD_NOALLOC_SCRATCH_BYTES
 DEVERR_BAD_QUERY_START_LOC = 0x1
 DEVERR_BAD_CACHE_INDEX = 0x2
 DEVERR_TIMEOUT = 0x4
@@ -55,6 +58,8 @@ def library() -> ctypes.CDLL:
                                         + [vp, sz, vp])
     lib.ssd_scan_varlen_fwd_profiled.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_profiled.argtypes = lib.ssd_scan_varlen_fwd.argtypes + [vp]
+    lib.ssd_scan_varlen_fwd_noalloc.restype = ctypes.c_int
+    lib.ssd_scan_varlen_fwd_noalloc.argtypes = lib.ssd_scan_varlen_fwd.argtypes[:21] + [vp]
     lib.ssd_scan_varlen_read_errors.restype = ctypes.c_int
     lib.ssd_scan_varlen_read_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ssd_status_string.restype = ctypes.c_char_p
@@ -161,6 +166,23 @@ def ssd_scan_varlen_fwd(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc
                    cache_indices, chunk_size, dt_softplus, workspace, stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_scan_varlen_fwd")
+
+
+def ssd_scan_varlen_fwd_noalloc(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
+                                has_initial_state, cache_indices, *, chunk_size: int,
+                                dt_softplus: bool = True, stream=None) -> None:
+    """The scan for callers that cannot allocate device memory: same as
+    ssd_scan_varlen_fwd without a workspace; the scratch is the library's
+    built-in NOALLOC_SCRATCH_BYTES array (sizes needing more raise SSDError
+    with status SSD_ERR_TOO_LARGE).  Calls that overlap on the GPU race on
+    that array; serialise them."""
+    import torch
+    args = _fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
+                     has_initial_state, cache_indices, chunk_size, dt_softplus,
+                     torch.empty(0, dtype=torch.uint8, device=x.device), stream)
+    st = library().ssd_scan_varlen_fwd_noalloc(*args[:21], args[23])
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan_varlen_fwd_noalloc")
 
 
 def ssd_scan_varlen_read_errors(workspace, stream=None) -> int:

@@ -93,6 +93,7 @@ const char *ssd_status_string(ssd_status_t s)
     case SSD_ERR_WORKSPACE: return "workspace missing or too small";
     case SSD_ERR_CUDA: return "CUDA error";
     case SSD_ERR_DEVICE: return "device-side error flag set";
+    case SSD_ERR_TOO_LARGE: return "sizes need more scratch than the built-in no-allocation buffer";
     }
     return "unknown status";
 }
@@ -115,7 +116,7 @@ int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
 
 }  // extern "C"
 
-namespace {
+namespace ssd {
 
 ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
                        const void *C, const float *D, const float *dt_bias, float *ssm_pool,
@@ -214,7 +215,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     return SSD_OK;
 }
 
-}  // namespace
+}  // namespace ssd
 
 extern "C" {
 
@@ -228,7 +229,7 @@ ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const f
                                  int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
                                  void *workspace, size_t workspace_bytes, ssd_stream_t stream)
 {
-    return scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
                      cache_indices, total_len, batch, nheads, head_dim, ngroups, dstate, max_slots,
                      chunk_size, dt_softplus, workspace, workspace_bytes, stream, nullptr);
 }
@@ -246,7 +247,7 @@ ssd_status_t ssd_scan_varlen_fwd_profiled(
     for (int k = 0; k < 5; ++k)
         if (!events[k])
             return SSD_ERR_INVALID_ARG;
-    return scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
                      cache_indices, total_len, batch, nheads, head_dim, ngroups, dstate, max_slots,
                      chunk_size, dt_softplus, workspace, workspace_bytes, stream, events);
 }

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/ssd_scan.h"
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -38,6 +39,17 @@ struct ChunkScanMaps {
 size_t chunk_scan_smem_bytes(const ScanParams &p);
 cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps,
                               cudaStream_t stream);
+
+// The whole scan (argument checks, tensor maps, the four launches) on a
+// caller-provided scratch buffer; `events` (5 CUDA events) may be null.
+ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
+                       const void *C, const float *D, const float *dt_bias, float *ssm_pool,
+                       const int32_t *query_start_loc, const uint8_t *has_initial_state,
+                       const uint32_t *cache_indices, int64_t total_len, int32_t batch,
+                       int32_t nheads, int32_t head_dim, int32_t ngroups, int32_t dstate,
+                       int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+                       void *workspace, size_t workspace_bytes, ssd_stream_t stream,
+                       void *const *events);
 
 inline int pad64(int v) { return (v + 63) / 64 * 64; }
 
