@@ -1,8 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark of the Mamba-2 SSD varlen forward prefill scan on GB300.
 
-One step = one ssd_scan_varlen_fwd call (all four stages: chunk table, chunk
-state, state passing, chunk scan) on the kernelindex-shaped workload: one
+One step = one ssd_scan_varlen_fwd call (all three launches: chunk state,
+state passing, chunk scan) on the kernelindex-shaped workload: one
 4096-token sequence, nheads=16, head_dim=64, ngroups=1, dstate=256, chunk 256
 (the head/state shape of the kernelindex "Mamba chunk scan with segsum"
 suite, whose cases are not published).  Inputs are seeded synthetic data
@@ -46,7 +46,7 @@ from mamba_ssd_chunked_varlen_gb300 import workloads as W  # noqa: E402
 METRIC = "SSD scan tokens/s and µs/call on 1 GB300; % of tensor/HBM roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
-STAGES = ("chunk_table", "chunk_state", "state_passing", "chunk_scan")
+STAGES = ("chunk_state", "state_passing", "chunk_scan")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -128,7 +128,6 @@ def work_model(w) -> dict:
         if not (first and not hinit[b]):
             f_off += H * l * N * P * 2
     stages = {
-        "chunk_table": {"bytes": (w.batch + 1) * 4 + w.batch * 4, "flops": 0},
         "chunk_state": {"bytes": x_b + bc_b + dt_b, "flops": f_state},
         "state_passing": {"bytes": pool_r + pool_w, "flops": 0},
         "chunk_scan": {"bytes": x_b + 2 * bc_b + dt_b + y_b, "flops": f_cb + f_diag + f_off},
@@ -310,9 +309,10 @@ def run_ours(args, rank, world, local):
     tokens_all = T * world
     value = tokens_all / (mean_ms_all * 1e-3)
 
-    # ---- per-stage attribution (stage events between the four launches)
+    # ---- per-stage attribution (stage events between the three launches)
     Kp = min(K, 500)
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(Kp)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(Kp)]
     for k in range(Kp):
         flush.fill_(k)
         pkg.ssd_scan_varlen_fwd_profiled(

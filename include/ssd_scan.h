@@ -102,9 +102,11 @@ SSD_API size_t ssd_scan_varlen_workspace_size(int64_t total_len, int32_t batch, 
  *
  * Only the pool slots named by cache_indices are written (each with the
  * final state of its sequence, also for a zero-length sequence); every other
- * pool byte is left unchanged.  Supported: 16 <= head_dim <= 128 and
- * 16 <= dstate <= 256, both multiples of 16; chunk_size in {64, 128, 256};
- * nheads % ngroups == 0.  x, B, C, y must be 16-byte aligned.
+ * pool byte is left unchanged.  Supported: head_dim in {16, 32, 64, 128},
+ * 16 <= dstate <= 256 a multiple of 16, chunk_size in {64, 128, 256},
+ * nheads % ngroups == 0.  x, B, C, y must be 16-byte aligned.  chunk_size
+ * only changes rounding: chunks longer than 128 tokens are processed as
+ * 128-token blocks with the state passed between them.
  * batch == 0 returns SSD_OK without launching.
  * Device-data preconditions (qsl monotone from 0 to total_len, slots in
  * range) are checked on the device; see SSD_DEVERR_*. */
@@ -116,13 +118,14 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd(
     int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
     void *workspace, size_t workspace_bytes, ssd_stream_t stream);
 
-/* ssd_scan_varlen_fwd with per-stage timing: `events` points to 5 CUDA events
+/* ssd_scan_varlen_fwd with per-stage timing: `events` points to 4 CUDA events
  * (cudaEvent_t, created by the caller) that are recorded on `stream` before
- * stage 0 and after each of the four stages (chunk table, chunk state, state
+ * the first stage and after each of the three launches (chunk state, state
  * passing, chunk scan); cudaEventElapsedTime between consecutive events gives
  * each stage's device time.  Otherwise identical to ssd_scan_varlen_fwd
- * (same arguments, results and errors).  The extra records put a small gap
- * between stages, so use it to attribute time, not to time the whole call. */
+ * (same arguments, results and errors).  The records separate the launches
+ * (no overlap between stages), so use it to attribute time, not to time the
+ * whole call. */
 SSD_API ssd_status_t ssd_scan_varlen_fwd_profiled(
     void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
     const float *D, const float *dt_bias, float *ssm_pool, const int32_t *query_start_loc,
@@ -132,9 +135,9 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd_profiled(
     void *workspace, size_t workspace_bytes, ssd_stream_t stream, void *const *events);
 
 /* Size of the scratch buffer built into the library for
- * ssd_scan_varlen_fwd_noalloc (32 MiB of device memory on every GPU that
+ * ssd_scan_varlen_fwd_noalloc (64 MiB of device memory on every GPU that
  * loads the library, held until the process exits). */
-#define SSD_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define SSD_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /* The scan for callers that cannot allocate device memory.  The pages have
  * no counterpart to this entry point; it exists for host code that may not
@@ -145,9 +148,8 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd_profiled(
  * Same arguments, results and errors as ssd_scan_varlen_fwd, minus the
  * workspace: the scratch lives in a fixed SSD_NOALLOC_SCRATCH_BYTES device
  * array inside the library.  Sizes whose ssd_scan_varlen_workspace_size
- * exceeds it return SSD_ERR_TOO_LARGE without launching (32 MiB fits, for
- * example, one 4096-token sequence with nheads 16, head_dim 64, dstate 256,
- * chunk 256).  The caller still passes every input and output.
+ * exceeds it return SSD_ERR_TOO_LARGE without launching (64 MiB fits, for
+ * example, one 4096-token sequence with nheads 16, head_dim 64, dstate 256).  The caller still passes every input and output.
  *
  * The first call on each device looks up that device's address of the array
  * (with the device current); make that first call before any stream capture.

@@ -27,7 +27,7 @@ EXPORTED_SYMBOLS = (
 
 SSD_OK = 0
 SSD_ERR_TOO_LARGE = 6
-NOALLOC_SCRATCH_BYTES = 32 << 20  # SSD_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 64 << 20  # SSD_NOALLOC_SCRATCH_BYTES
 DEVERR_BAD_QUERY_START_LOC = 0x1
 DEVERR_BAD_CACHE_INDEX = 0x2
 DEVERR_TIMEOUT = 0x4
@@ -133,15 +133,15 @@ def ssd_scan_varlen_fwd_profiled(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_
                                  has_initial_state, cache_indices, *, chunk_size: int,
                                  dt_softplus: bool = True, workspace=None, stream=None,
                                  events=None) -> None:
-    """ssd_scan_varlen_fwd that also records 5 torch.cuda.Event objects around
-    the four stages (chunk table, chunk state, state passing, chunk scan)."""
-    if events is None or len(events) != 5:
-        raise ValueError("events must be 5 torch.cuda.Event objects")
+    """ssd_scan_varlen_fwd that also records 4 torch.cuda.Event objects around
+    the three launches (chunk state, state passing, chunk scan)."""
+    if events is None or len(events) != 4:
+        raise ValueError("events must be 4 torch.cuda.Event objects")
     import torch
     for e in events:
         if e.cuda_event == 0:  # torch creates the CUDA event lazily, on first record
             e.record(torch.cuda.current_stream() if stream is None else stream)
-    handles = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     st = library().ssd_scan_varlen_fwd_profiled(
         *_fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
                    cache_indices, chunk_size, dt_softplus, workspace, stream), handles)

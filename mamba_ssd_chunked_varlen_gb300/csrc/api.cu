@@ -63,19 +63,18 @@ ssd_status_t check_sizes(int64_t T, int32_t batch, int32_t H, int32_t P, int32_t
         return SSD_ERR_INVALID_ARG;
     if (N > SSD_MAX_DSTATE)
         return SSD_ERR_UNSUPPORTED;
-    if (P % 16 != 0 || P > 128 || N % 16 != 0)
+    if ((P != 16 && P != 32 && P != 64 && P != 128) || N % 16 != 0 || N < 16)
         return SSD_ERR_UNSUPPORTED;
     if (Q != 64 && Q != 128 && Q != 256)
         return SSD_ERR_UNSUPPORTED;
     if (T > INT32_MAX / 2 || static_cast<int64_t>(batch) > INT32_MAX / 2)
         return SSD_ERR_UNSUPPORTED;
-    ScanParams probe;
-    std::memset(&probe, 0, sizeof probe);
-    probe.P = P;
-    probe.N = N;
-    probe.Q = Q;
-    if (ssd::chunk_state_smem_bytes(probe) > static_cast<size_t>(ssd::kMaxSmemPerBlock) ||
-        ssd::chunk_scan_smem_bytes(probe) > static_cast<size_t>(ssd::kMaxSmemPerBlock))
+    const ssd::K1Config k1 = ssd::chunk_state_config(H, G, P, N);
+    const ssd::K3Config k3 = ssd::chunk_scan_config(H, G, P, N);
+    if (k1.HB == 0 || k3.HB == 0)
+        return SSD_ERR_UNSUPPORTED;
+    if (k1.smem > static_cast<size_t>(ssd::kMaxSmemPerBlock) ||
+        k3.smem > static_cast<size_t>(ssd::kMaxSmemPerBlock))
         return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
 }
@@ -104,14 +103,15 @@ size_t ssd_scan_varlen_workspace_size(int64_t total_len, int32_t batch, int32_t 
 {
     if (check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size) != SSD_OK)
         return 0;
-    return ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, chunk_size).total;
+    return ssd::ws_layout(total_len, batch, nheads, head_dim, dstate,
+                          ssd::block_tokens(chunk_size)).total;
 }
 
 int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
 {
     if (batch <= 0)
         return 0;
-    return total_len > 0 ? 4 : 2;
+    return total_len > 0 ? 3 : 2;
 }
 
 }  // extern "C"
@@ -143,8 +143,8 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
         return SSD_ERR_INVALID_ARG;
     if (!aligned16(ssm_pool))
         return SSD_ERR_INVALID_ARG;
-    const ssd::WsLayout L =
-        ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, chunk_size);
+    const int32_t Qb = ssd::block_tokens(chunk_size);
+    const ssd::WsLayout L = ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, Qb);
     if (!workspace || workspace_bytes < L.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return SSD_ERR_WORKSPACE;
@@ -171,46 +171,48 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.P = head_dim;
     p.G = ngroups;
     p.N = dstate;
-    p.Q = chunk_size;
+    p.Q = Qb;
     p.max_slots = max_slots;
     p.dt_softplus = dt_softplus ? 1 : 0;
     p.max_chunks = static_cast<int32_t>(L.max_chunks);
     p.hdr = reinterpret_cast<ssd::WsHeader *>(ws + L.header);
-    p.chunks = reinterpret_cast<ssd::ChunkEntry *>(ws + L.chunks);
     p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);
-    p.dtp = reinterpret_cast<float *>(ws + L.dtp);
-    p.acum = reinterpret_cast<float *>(ws + L.acum);
+    p.decay = reinterpret_cast<float *>(ws + L.decay);
     p.schunk = reinterpret_cast<float *>(ws + L.schunk);
     p.sprev = reinterpret_cast<__nv_bfloat16 *>(ws + L.sprev);
 
     ssd::ChunkStateMaps m1;
     ssd::ChunkScanMaps m3;
+    std::memset(&m1, 0, sizeof m1);  // with total_len == 0 no kernel reads a map
+    std::memset(&m3, 0, sizeof m3);
     if (total_len > 0) {
         const uint64_t T = static_cast<uint64_t>(total_len);
         const uint64_t H = nheads, P = head_dim, G = ngroups, N = dstate;
         bool ok = make_map_3d(&m1.B, B, N, G, T, N * 2, G * N * 2, 1, 64) &&
+                  make_map_3d(&m1.X, x, H * P, T, 1, H * P * 2, H * P * T * 2, 64, 1) &&
                   make_map_3d(&m3.B, B, N, G, T, N * 2, G * N * 2, 1, 64) &&
                   make_map_3d(&m3.C, C, N, G, T, N * 2, G * N * 2, 1, 64) &&
-                  make_map_3d(&m3.X, x, P, H, T, P * 2, H * P * 2, 1, 64) &&
+                  make_map_3d(&m3.X, x, H * P, T, 1, H * P * 2, H * P * T * 2, 64, 1) &&
                   make_map_3d(&m3.Sprev, p.sprev, N, P, static_cast<uint64_t>(L.max_chunks) * H,
                               N * 2, P * N * 2, 64, 1);
         if (!ok)
             return SSD_ERR_CUDA;
     }
 
+    // Stage events (profiled entry point): before the first launch and after
+    // each launch.  Between launches they also end the programmatic overlap.
     auto mark = [&](int k) {
         return events == nullptr ||
                cudaEventRecord(static_cast<cudaEvent_t>(events[k]), stream) == cudaSuccess;
     };
-    if (!mark(0) || ssd::launch_chunk_table(p, stream) != cudaSuccess || !mark(1))
+    const bool pdl = events == nullptr;
+    if (!mark(0) || ssd::launch_chunk_state(p, m1, stream) != cudaSuccess || !mark(1))
         return SSD_ERR_CUDA;
-    if (total_len > 0 && ssd::launch_chunk_state(p, m1, stream) != cudaSuccess)
+    if (ssd::launch_state_passing(p, stream, pdl) != cudaSuccess || !mark(2))
         return SSD_ERR_CUDA;
-    if (!mark(2) || ssd::launch_state_passing(p, stream) != cudaSuccess || !mark(3))
+    if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream, pdl) != cudaSuccess)
         return SSD_ERR_CUDA;
-    if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream) != cudaSuccess)
-        return SSD_ERR_CUDA;
-    if (!mark(4))
+    if (!mark(3))
         return SSD_ERR_CUDA;
     return SSD_OK;
 }
@@ -244,7 +246,7 @@ ssd_status_t ssd_scan_varlen_fwd_profiled(
 {
     if (!events)
         return SSD_ERR_INVALID_ARG;
-    for (int k = 0; k < 5; ++k)
+    for (int k = 0; k < 4; ++k)
         if (!events[k])
             return SSD_ERR_INVALID_ARG;
     return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,

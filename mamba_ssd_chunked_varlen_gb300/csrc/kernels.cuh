@@ -12,33 +12,44 @@
 
 namespace ssd {
 
-// Stage 0: chunk table from query_start_loc, device-side argument checks.
-cudaError_t launch_chunk_table(const ScanParams &p, cudaStream_t stream);
-
-// Stage 1+2c: per (chunk, head) processed dt, cumulative log-decay and the
-// chunk state  S_c[p][n] = sum_j exp(Acum_last - Acum_j) dt_j x[j,p] B[j,n].
+// Stages 1+2c: per (block, head group) processed dt, cumulative log-decay and
+// the block state  S_c[p][n] = sum_j exp(Acum_last - Acum_j) dt_j x[j,p] B[j,n];
+// also the per-sequence first-block table and the error word.
 struct ChunkStateMaps {
     CUtensorMap B;  // bf16 (N, G, T), box {64, 1, 64}, 128-byte swizzle
+    CUtensorMap X;  // bf16 (H*P, T, 1), box {64, 64, 1}
 };
-size_t chunk_state_smem_bytes(const ScanParams &p);
+struct K1Config {
+    int HB, NP, n_mtiles;
+    uint32_t tmem_cols;
+    size_t smem;
+};
+K1Config chunk_state_config(int H, int G, int P, int N);
 cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
                                cudaStream_t stream);
 
-// Stage 3: inter-chunk state passing; writes the state entering every chunk
-// and the final state of every sequence into its pool slot.
-cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream);
+// Stage 3: inter-block state passing; writes the state entering every block
+// and the final state of every sequence into its pool slot.  `programmatic`:
+// launched as a programmatic dependent of the previous kernel.
+cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool programmatic);
 
-// Stage 2a/2b/4: per (chunk, 128-row tile, head) C.B^T, the masked diagonal
-// block, the off-diagonal C.S_prev^T term and the D skip; writes y.
+// Stages 2a/2b/4: per (block, head group) C.B^T, the masked diagonal block,
+// the off-diagonal C.S_prev^T term and the D skip; writes y.
 struct ChunkScanMaps {
     CUtensorMap C;      // bf16 (N, G, T), box {64, 1, 64}
     CUtensorMap B;      // bf16 (N, G, T), box {64, 1, 64}
-    CUtensorMap X;      // bf16 (P, H, T), box {64, 1, 64}
-    CUtensorMap Sprev;  // bf16 (N, P, chunks*H), box {64, 64, 1}
+    CUtensorMap X;      // bf16 (H*P, T, 1), box {64, 64, 1}
+    CUtensorMap Sprev;  // bf16 (N, P, blocks*H), box {64, 64, 1}
 };
-size_t chunk_scan_smem_bytes(const ScanParams &p);
-cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps,
-                              cudaStream_t stream);
+struct K3Config {
+    int HB;          // heads per CTA (one group)
+    int P_pad, N_pad;
+    int nS, nX, nY;  // ring depths: S_prev tiles, X tiles, TMEM accumulator slots
+    size_t smem;
+};
+K3Config chunk_scan_config(int H, int G, int P, int N);
+cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps, cudaStream_t stream,
+                              bool programmatic);
 
 // The whole scan (argument checks, tensor maps, the four launches) on a
 // caller-provided scratch buffer; `events` (5 CUDA events) may be null.

@@ -17,17 +17,10 @@ constexpr uint32_t kErrTimeout = 0x4u;
 // Limit for every on-chip wait (mbarrier) before the kernel gives up.
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
 
-// Chunk table entry: one chunk of one sequence, aligned to the sequence start.
-//   x = sequence index, y = first token, z = length (1..chunk_size),
-//   w = flags (bit 0: first chunk of its sequence, bit 1: last chunk).
-using ChunkEntry = int4;
-constexpr int kChunkFirst = 1;
-constexpr int kChunkLast = 2;
-
 // Header words at the start of the workspace.
 struct WsHeader {
     uint32_t errors;   // SSD_DEVERR_* bits of the current call
-    int32_t nchunks;   // chunks in the table
+    int32_t nchunks;   // blocks of the call
     int32_t valid;     // 1 when query_start_loc passed the device checks
     int32_t pad[61];
 };
@@ -36,17 +29,25 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 // Byte offsets of the workspace regions; every region is 256-byte aligned.
 struct WsLayout {
     int64_t max_chunks;
-    size_t header, chunks, seq_first, dtp, acum, schunk, sprev, total;
+    size_t header, seq_first, decay, schunk, sprev, total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Upper bound on the number of chunks: sum_b ceil(L_b / Q) <= ceil(T / Q) + batch.
+// Tokens per block: chunks longer than 128 tokens are processed as 128-token
+// blocks (the chunked form is exact at any chunk size).
+__host__ __device__ inline int32_t block_tokens(int32_t chunk_size)
+{
+    return chunk_size < 128 ? chunk_size : 128;
+}
+
+// Upper bound on the number of blocks: sum_b ceil(L_b / Q) <= ceil(T / Q) + batch.
 __host__ __device__ inline int64_t max_chunks_bound(int64_t T, int32_t batch, int32_t Q)
 {
     return (T + Q - 1) / Q + batch;
 }
 
+// Q here is the block size (block_tokens of the chunk size).
 __host__ __device__ inline WsLayout ws_layout(int64_t T, int32_t batch, int32_t H, int32_t P,
                                               int32_t N, int32_t Q)
 {
@@ -56,14 +57,10 @@ __host__ __device__ inline WsLayout ws_layout(int64_t T, int32_t batch, int32_t 
     size_t off = 0;
     L.header = off;
     off = align256(off + sizeof(WsHeader));
-    L.chunks = off;
-    off = align256(off + sizeof(ChunkEntry) * (mc + 1));
     L.seq_first = off;
     off = align256(off + sizeof(int32_t) * (static_cast<size_t>(batch) + 1));
-    L.dtp = off;
-    off = align256(off + sizeof(float) * mc * H * Q);
-    L.acum = off;
-    off = align256(off + sizeof(float) * mc * H * Q);
+    L.decay = off;
+    off = align256(off + sizeof(float) * mc * H);
     L.schunk = off;
     off = align256(off + sizeof(float) * mc * H * P * N);
     L.sprev = off;
@@ -85,18 +82,17 @@ struct ScanParams {
     const uint8_t *has_init;  // may be null
     const uint32_t *cache_idx;
     int64_t T;
-    int32_t batch, H, P, G, N, Q;
+    int32_t batch, H, P, G, N;
+    int32_t Q;            // tokens per block (block_tokens of the chunk size)
     int64_t max_slots;
     int32_t dt_softplus;
-    int32_t max_chunks;
+    int32_t max_chunks;   // upper bound on the number of blocks
     // workspace regions
     WsHeader *hdr;
-    ChunkEntry *chunks;
-    int32_t *seq_first;   // (batch + 1): first chunk of each sequence, then the total
-    float *dtp;           // [chunk][head][Q] processed dt (0 past the chunk end)
-    float *acum;          // [chunk][head][Q] inclusive cumulative A*dt within the chunk
-    float *schunk;        // [chunk][head][P][N] chunk states (zero initial state)
-    __nv_bfloat16 *sprev; // [chunk][head][P][N] state entering each chunk (bf16 operand)
+    int32_t *seq_first;   // (batch + 1): first block of each sequence, then the total
+    float *decay;         // [block][head] exp(sum of A*dt over the block)
+    float *schunk;        // [block][head][P][N] block states (zero initial state)
+    __nv_bfloat16 *sprev; // [block][head][P][N] state entering each block (bf16 operand)
 };
 
 __device__ __forceinline__ void record_error(WsHeader *hdr, uint32_t flag)

@@ -1,0 +1,144 @@
+// Device helpers shared by the scan kernels: programmatic dependent launch,
+// block scans, mapping of a block index to its sequence, dt processing.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "ssd_common.cuh"
+
+namespace ssd {
+
+// ---------------------------------------------------------------- PDL
+// Lets the next kernel in the stream start launching (its CTAs run their
+// prologue and then block in pdl_wait()).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until the previous kernel in the stream has completed and its memory
+// writes are visible (a no-op when the launch was not programmatic).
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- math
+__device__ __forceinline__ float softplus_f32(float v)
+{
+    return v > 20.f ? v : log1pf(expf(v));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// Processed step of token t, head h: softplus(dt + dt_bias) (or dt + dt_bias).
+__device__ __forceinline__ float processed_dt(const ScanParams &p, int64_t t, int h)
+{
+    float v = __bfloat162float(p.dt[t * p.H + h]);
+    if (p.dt_bias)
+        v += p.dt_bias[h];
+    return p.dt_softplus ? softplus_f32(v) : v;
+}
+
+// Inclusive scan over the 32 lanes of a warp.
+template <typename T>
+__device__ __forceinline__ T warp_inclusive_scan(T v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const T t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o)
+            v += t;
+    }
+    return v;
+}
+
+// ---------------------------------------------------------------- block map
+// Where a block (at most `blk_len` tokens of one sequence, aligned to the
+// sequence start) lies: blocks are numbered sequence after sequence.
+struct BlockInfo {
+    int32_t seq;     // sequence index, or -1 when the block index is past the end
+    int32_t t0;      // first token
+    int32_t len;     // tokens in the block (1..blk_len)
+    int32_t first;   // 1 when this is the sequence's first block
+    int32_t valid;   // 0 when query_start_loc failed the checks
+    int32_t total;   // number of blocks of the whole call
+};
+
+// Maps block `blk` by scanning query_start_loc.  Called by every thread of a
+// CTA of kThreads threads (kThreads a multiple of 32, <= 1024); uses `scratch`
+// (>= 40 ints of shared memory).  When `seq_first` is non-null the CTA also
+// writes every sequence's first block index there (and the total at [batch]).
+// One pass over query_start_loc per kThreads sequences: the checks of its
+// first and last entries ride along with the loads of the scan.
+template <int kThreads>
+__device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratch,
+                               int32_t *seq_first)
+{
+    constexpr int kWarps = kThreads / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t *s_warp = scratch;        // kWarps partial sums
+    int32_t *s_res = scratch + 32;    // 4 result ints, written by the owning thread
+    int32_t carry = 0;
+    int bad = 0;
+    for (int base = 0; base < p.batch; base += kThreads) {
+        const int b = base + tid;
+        int32_t start = 0, len = 0, n = 0;
+        if (b < p.batch) {
+            start = p.qsl[b];
+            const int32_t end = p.qsl[b + 1];
+            len = end - start;
+            if (len < 0 || (b == 0 && start != 0) ||
+                (b == p.batch - 1 && static_cast<int64_t>(end) != p.T)) {
+                bad = 1;
+                len = 0;
+            }
+            n = (len + p.Q - 1) / p.Q;
+        }
+        const int32_t incl = warp_inclusive_scan(n);
+        if (lane == 31)
+            s_warp[warp] = incl;
+        __syncthreads();
+        int32_t before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int32_t v = s_warp[w];
+            before += w < warp ? v : 0;
+            total += v;
+        }
+        const int32_t first = carry + before + incl - n;
+        if (b < p.batch) {
+            if (seq_first)
+                seq_first[b] = first;
+            if (blk >= first && blk < first + n) {
+                const int32_t k = static_cast<int32_t>(blk - first);
+                s_res[0] = b;
+                s_res[1] = start + k * p.Q;
+                s_res[2] = min(p.Q, len - k * p.Q);
+                s_res[3] = k == 0;
+            }
+        }
+        carry += total;
+        __syncthreads();
+    }
+    if (seq_first && tid == 0)
+        seq_first[p.batch] = carry;
+    bad = __syncthreads_or(bad);
+    BlockInfo bi;
+    bi.valid = !bad;
+    bi.total = carry;
+    const bool mine = !bad && blk < carry;
+    bi.seq = mine ? s_res[0] : -1;
+    bi.t0 = mine ? s_res[1] : 0;
+    bi.len = mine ? s_res[2] : 0;
+    bi.first = mine ? s_res[3] : 0;
+    return bi;
+}
+
+}  // namespace ssd

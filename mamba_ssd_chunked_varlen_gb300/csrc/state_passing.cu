@@ -3,24 +3,34 @@
 // with segsum").  For every sequence b and head h:
 //
 //   S   = has_initial_state[b] ? ssm_pool[slot][h] : 0
-//   for each chunk c of b:  S_prev[c] = S;   S = exp(Acum_last(c)) * S + S_c[c]
+//   for each block c of b:  S_prev[c] = S;   S = decay_c * S + S_c[c]
 //   ssm_pool[slot][h] = S                      (in-place write-back, page
 //                                               "Mamba2SSDChunkScanVarlenFwdInplace")
 //
 // Every (p, n) element is an independent chain, so the grid covers the
 // head_dim x dstate elements of every (sequence, head) with 4 elements per
-// thread; the per-chunk loads do not depend on the running state and are
-// issued ahead of the FMAs.  HBM/L2-bandwidth bound.
+// thread; the block states and decays of several blocks are loaded before
+// any of them is used.  L2/HBM-bandwidth bound.  Launched as a programmatic
+// dependent of the chunk-state kernel: it waits for that grid before reading.
 #include "kernels.cuh"
+#include "ssd_device.cuh"
+#include "trace.cuh"
 
 namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVec = 4;
+constexpr int kAhead = 8;  // blocks loaded ahead of use
 
 __global__ void __launch_bounds__(kThreads) state_passing_kernel(ScanParams p, int blocks_per_head)
 {
+    if (threadIdx.x == 0)
+        SSD_TRACE_EV(1, 0);
+    pdl_launch_dependents();
+    pdl_wait();
+    if (threadIdx.x == 0)
+        SSD_TRACE_EV(1, 1);
     if (!p.hdr->valid)
         return;
     const int b = blockIdx.x / blocks_per_head;
@@ -41,35 +51,60 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(ScanParams p, i
         S = *reinterpret_cast<const float4 *>(pool_h);
 
     const int c_begin = p.seq_first[b], c_end = p.seq_first[b + 1];
-    for (int c = c_begin; c < c_end; ++c) {
-        const int64_t off = (static_cast<int64_t>(c) * p.H + h) * PN + e;
-        const float4 sc = *reinterpret_cast<const float4 *>(p.schunk + off);
-        const int len = p.chunks[c].z;
-        const float decay = expf(p.acum[(static_cast<int64_t>(c) * p.H + h) * p.Q + len - 1]);
-        __nv_bfloat162 lo = __floats2bfloat162_rn(S.x, S.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(S.z, S.w);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t *>(&lo);
-        packed.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(p.sprev + off) = packed;
-        S.x = fmaf(decay, S.x, sc.x);
-        S.y = fmaf(decay, S.y, sc.y);
-        S.z = fmaf(decay, S.z, sc.z);
-        S.w = fmaf(decay, S.w, sc.w);
+    const int64_t stride = static_cast<int64_t>(p.H) * PN;
+    const float *__restrict__ sc = p.schunk + (static_cast<int64_t>(c_begin) * p.H + h) * PN + e;
+    __nv_bfloat16 *__restrict__ sp = p.sprev + (static_cast<int64_t>(c_begin) * p.H + h) * PN + e;
+    const float *__restrict__ dec = p.decay + static_cast<int64_t>(c_begin) * p.H + h;
+    for (int c = c_begin; c < c_end; c += kAhead) {
+        float4 v[kAhead];
+        float d[kAhead];
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            if (c + k < c_end) {
+                v[k] = __ldg(reinterpret_cast<const float4 *>(sc + k * stride));
+                d[k] = __ldg(dec + static_cast<int64_t>(k) * p.H);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            if (c + k < c_end) {
+                uint2 packed;
+                packed.x = pack_bf16(S.x, S.y);
+                packed.y = pack_bf16(S.z, S.w);
+                *reinterpret_cast<uint2 *>(sp + k * stride) = packed;
+                S.x = fmaf(d[k], S.x, v[k].x);
+                S.y = fmaf(d[k], S.y, v[k].y);
+                S.z = fmaf(d[k], S.z, v[k].z);
+                S.w = fmaf(d[k], S.w, v[k].w);
+            }
+        }
+        sc += kAhead * stride;
+        sp += kAhead * stride;
+        dec += static_cast<int64_t>(kAhead) * p.H;
     }
     if (slot_ok)
         *reinterpret_cast<float4 *>(pool_h) = S;
+    if (threadIdx.x == 0)
+        SSD_TRACE_EV(1, 2);
 }
 
 }  // namespace
 
-cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream)
+cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool programmatic)
 {
     const int64_t PN = static_cast<int64_t>(p.P) * p.N;
     const int blocks_per_head = static_cast<int>((PN / kVec + kThreads - 1) / kThreads);
-    dim3 grid(static_cast<unsigned>(blocks_per_head) * p.batch, p.H);
-    state_passing_kernel<<<grid, kThreads, 0, stream>>>(p, blocks_per_head);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks_per_head) * p.batch, p.H);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, state_passing_kernel, p, blocks_per_head);
 }
 
 }  // namespace ssd

@@ -44,20 +44,23 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     ws = binding.ssd_scan_varlen_workspace_size
     n1 = ws(4096, 1, 16, 64, 1, 256, 256)
-    # chunk states dominate: (ceil(T/Q) + batch) chunks x H x P x N x (4 + 2) bytes
-    assert n1 >= 17 * 16 * 64 * 256 * 6
-    assert n1 < 17 * 16 * 64 * 256 * 6 + 17 * 16 * 256 * 8 + 64 * 1024
+    # block states dominate: (ceil(T/128) + batch) blocks x H x P x N x (4 + 2) bytes
+    # (chunks longer than 128 tokens are processed as 128-token blocks)
+    assert n1 >= 33 * 16 * 64 * 256 * 6
+    assert n1 < 33 * 16 * 64 * 256 * 6 + 64 * 1024
+    assert ws(4096, 1, 16, 64, 1, 256, 128) == n1
     assert ws(4096, 2, 16, 64, 1, 256, 256) > n1          # more sequences, more chunks
     assert ws(0, 3, 4, 32, 1, 32, 64) > 0                 # empty sequences still need a table
     assert ws(512, 1, 4, 32, 1, 512, 64) == 0             # dstate > 256 (MAX_DSTATE)
     assert ws(512, 1, 4, 32, 1, 32, 100) == 0             # unsupported chunk size
     assert ws(512, 1, 6, 32, 4, 32, 64) == 0              # nheads % ngroups != 0
     assert ws(512, 1, 4, 24, 1, 32, 64) == 0              # head_dim not a multiple of 16
+    assert ws(512, 1, 4, 48, 1, 32, 64) == 0              # head_dim not a power of two
     assert ws(512, 1, 4, 256, 1, 32, 64) == 0             # head_dim > 128
 
 
 def test_launch_count(lib):
-    assert binding.ssd_scan_varlen_num_launches(4096, 1) == 4
+    assert binding.ssd_scan_varlen_num_launches(4096, 1) == 3
     assert binding.ssd_scan_varlen_num_launches(0, 3) == 2
     assert binding.ssd_scan_varlen_num_launches(10, 0) == 0
 
