@@ -13,12 +13,12 @@
 // "mamba2_ssd_scan".  A block is at most 128 tokens of one sequence (one MMA
 // tile of rows); CB is computed once per block and shared by the CTA's heads.
 //
-// Warp roles (one CTA, 10 warps), heads processed as a pipeline:
+// Warp roles (one CTA, 18 warps), heads processed as a pipeline:
 //   warp 0    TMA producer: X of the first heads, C and B, then per head its
 //             S_prev (after the state-passing kernel) and the next head's X
 //   warp 1    tcgen05 issuer: CB once; per head Ydiag = Ldt X and Yoff = C S_prev^T
 //             into a TMEM accumulator slot
-//   warps 2-9 dt and cumulative decay; per head the masked Ldt tile (CB read
+//   warps 2-17 dt and cumulative decay; per head the masked Ldt tile (CB read
 //             from TMEM, written to shared memory as a bf16 operand) and the
 //             epilogue of the previous head (overlapping the MMAs of this one)
 // C stays resident for every head's Yoff; S_prev tiles reuse B's space once
@@ -38,9 +38,9 @@
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kMathThreads = 256;     // warps 2..9
-constexpr int kMathWarps = 8;
+constexpr int kThreads = 576;
+constexpr int kMathThreads = 512;     // warps 2..17
+constexpr int kMathWarps = 16;
 constexpr int kRows = 128;
 constexpr int kBlk16 = kRows * 128;   // 128 rows x 128 B swizzled block (16 KB)
 constexpr int kNumBars = 16;
@@ -304,30 +304,30 @@ __global__ void __launch_bounds__(kThreads)
         }
     } else {
         // ------------------------------------------------------------ math warps
-        const int mt = tid - 64;             // 0..255
-        const int mw = warp - 2;             // math warp 0..7
-        const int mhalf = mt >> 7, jj = mt & 127;
+        const int mt = tid - 64;             // 0..511
+        const int mw = warp - 2;             // math warp 0..15
+        const int quarter = mt >> 7, jj = mt & 127;
         // dt of every head of the CTA at once (one round trip), then the scans
-        float dv[4];
+        float dv[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int hh = 2 * k + mhalf;
+        for (int k = 0; k < 2; ++k) {
+            const int hh = 4 * k + quarter;
             dv[k] = (hh < HB && jj < len) ? processed_dt(p, t0 + jj, h0 + hh) : 0.f;
         }
         if (mt == 0)
             SSD_TRACE_EV(2, 23);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (2 * k >= HB)
+        for (int k = 0; k < 2; ++k) {
+            if (4 * k >= HB)
                 break;
-            const int hh = 2 * k + mhalf;
+            const int hh = 4 * k + quarter;
             const float a = hh < HB ? p.A[h0 + hh] * dv[k] : 0.f;
             const float incl = warp_inclusive_scan(a);
             if (lane == 31)
                 s_part[mw] = incl;
             math_barrier();
             float before = 0.f;
-            for (int w = mhalf * 4; w < mw; ++w)
+            for (int w = quarter * 4; w < mw; ++w)
                 before += s_part[w];
             if (hh < HB) {
                 sDt[hh * kRows + jj] = dv[k];
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads)
         const int q = warp & 3;
         const int i = q * 32 + lane;          // block-local row of this thread
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const int col_base = mhalf * 64;      // this thread's 64 CB columns
+        const int col_base = quarter * 32;    // this thread's 32 CB columns
         bool ok = ptx::mbar_wait(bars + kCBDone, 0, kWaitTimeoutNs);
         if (mt == 0)
             SSD_TRACE_EV(2, 12);
@@ -364,9 +364,9 @@ __global__ void __launch_bounds__(kThreads)
             const float Dh = p.D ? p.D[h0 + hh] : 0.f;
             const int xoff = (h0 + hh) * p.P - x_col0(hh);   // head's first column in its X slot
             const uint8_t *xsl = sX + xs * L.x_slot;
-            const int ncols = P_pad / 2;
+            const int ncols = P_pad / 4;
 #pragma unroll 1
-            for (int col = mhalf * ncols; col < (mhalf + 1) * ncols; col += 16) {
+            for (int col = quarter * ncols; col < (quarter + 1) * ncols; col += 16) {
                 if (col >= p.P)
                     break;
                 float yd[16], yo[16];
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads)
                 // the math warps' code does not crowd the MMA issuer's out of the
                 // instruction cache they share
 #pragma unroll 1
-                for (int c16 = 0; c16 < 4; ++c16) {
+                for (int c16 = 0; c16 < 2; ++c16) {
                     const int col = col_base + c16 * 16;
                     float v[16];
                     ptx::tmem_ld16(tmem + lane_off + col, v);

@@ -15,19 +15,15 @@
 // the tcgen05 tensor cores, for several heads of one group at once:
 //   S^T[n, (h,p)] = sum_j Bmat[j, n] * (w_j,h x[j, h, p])
 // M = dstate (tiles of 128), N = heads x head_dim (<= 256), K = tokens.  B and
-// x arrive by TMA (MN-major, 128-byte swizzle).  Both operands are turned into
-// fp16 in place, each with a power-of-two scale chosen from its largest
-// magnitude (largest value in [2^14, 2^15)), so that fp16's range holds them
-// and its 11-bit significand rounds w x with relative error <= 2^-11; B itself
-// converts exactly.  One bf16 rounding of w x would leave ~1e-3 relative error
-// in final states; this leaves ~3e-4.  The scales are removed exactly in the
-// epilogue.  The CTA maps its block to its sequence itself, and CTA (0,0)
-// writes the per-sequence first-block table and resets the error word.
+// x arrive by TMA (MN-major, 128-byte swizzle); B is used as it is, shared by
+// the heads.  The weighted operand w_j x_j is formed by the threads in place
+// of x and split into bf16 hi + lo parts (two MMAs into one fp32 accumulator):
+// one bf16 rounding of w x would leave ~1e-3 relative error in final states,
+// the split leaves ~2^-17.  The CTA maps its block to its sequence itself, and
+// CTA (0,0) writes the per-sequence first-block table and resets the error word.
 //
 // Block states are stored [block][head][p][n] like the pool's slots, so the
 // state-passing kernel reads and writes both with the same coalesced pattern.
-#include <cuda_fp16.h>
-
 #include "kernels.cuh"
 #include "sm100_ptx.cuh"
 #include "ssd_device.cuh"
@@ -36,12 +32,12 @@
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kRows = 128;                     // tokens per block (max)
 constexpr int kNBlockBytes = kRows * 128;      // one 64-wide block of 128 rows (16 KB)
 
 struct K1Layout {
-    uint32_t sB, sW, sDt, sAcum, sWt, scratch, bars, tmem_slot, total;
+    uint32_t sB, sW, sLo, sDt, sAcum, sWt, scratch, bars, tmem_slot, total;
 };
 
 __host__ __device__ inline K1Layout k1_layout(int NP, int n_mtiles, int HB)
@@ -51,6 +47,8 @@ __host__ __device__ inline K1Layout k1_layout(int NP, int n_mtiles, int HB)
     L.sB = off;
     off += n_mtiles * 2 * kNBlockBytes;
     L.sW = off;
+    off += (NP / 64) * kNBlockBytes;
+    L.sLo = off;
     off += (NP / 64) * kNBlockBytes;
     L.sDt = off;
     off += HB * kRows * 4;
@@ -68,42 +66,6 @@ __host__ __device__ inline K1Layout k1_layout(int NP, int n_mtiles, int HB)
     return L;
 }
 
-// Largest |value| of a CTA-wide set: every thread passes its partial maximum.
-__device__ __forceinline__ float block_max(float v, float *s_red)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0)
-        s_red[warp] = v;
-    __syncthreads();
-    float m = 0.f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w)
-        m = fmaxf(m, s_red[w]);
-    __syncthreads();
-    return m;
-}
-
-// Exponent e such that max * 2^e lies in [2^14, 2^15) (0 for max == 0),
-// clamped so that the scale stays a finite fp32 power of two.
-__device__ __forceinline__ int fp16_scale_exp(float max_abs)
-{
-    if (!(max_abs > 0.f))
-        return 0;
-    int ex;
-    frexpf(max_abs, &ex);  // max = f * 2^ex, f in [0.5, 1)
-    int e = 15 - ex;
-    return e > 100 ? 100 : (e < -100 ? -100 : e);
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float a, float b)
-{
-    __half2 t = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&t);
-}
-
 __global__ void __launch_bounds__(kThreads)
     chunk_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
                        ScanParams p, int HB, int NP, int n_mtiles, uint32_t tmem_cols)
@@ -114,6 +76,7 @@ __global__ void __launch_bounds__(kThreads)
     const K1Layout L = k1_layout(NP, n_mtiles, HB);
     uint8_t *sB = smem + L.sB;
     uint8_t *sW = smem + L.sW;
+    uint8_t *sLo = smem + L.sLo;
     float *sDt = reinterpret_cast<float *>(smem + L.sDt);
     float *sAcum = reinterpret_cast<float *>(smem + L.sAcum);
     float *sWt = reinterpret_cast<float *>(smem + L.sWt);
@@ -122,8 +85,7 @@ __global__ void __launch_bounds__(kThreads)
     uint64_t *bar_x = bar_b + 1;
     uint64_t *bar_mma = bar_b + 2;   // one per state tile (n_mtiles <= 2)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
-    float *s_part = reinterpret_cast<float *>(scratch + 40);  // 8 warp partials
-    float *s_red = reinterpret_cast<float *>(scratch + 48);   // 8 warp maxima
+    float *s_part = reinterpret_cast<float *>(scratch + 40);  // 16 warp partials
 
     const int blk = blockIdx.x;
     const int h0 = blockIdx.y * HB;
@@ -182,26 +144,26 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---- dt, softplus, cumulative A*dt per head: every head's dt loaded at
-    //      once (one round trip), then two heads per scan pass ----
-    const int half = tid >> 7, j = tid & 127;
-    float dv[4];
+    //      once (one round trip), then four heads per scan pass ----
+    const int quarter = tid >> 7, j = tid & 127;
+    float dv[2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int hh = 2 * k + half;
+    for (int k = 0; k < 2; ++k) {
+        const int hh = 4 * k + quarter;
         dv[k] = (hh < HB && j < len) ? processed_dt(p, t0 + j, h0 + hh) : 0.f;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (2 * k >= HB)
+    for (int k = 0; k < 2; ++k) {
+        if (4 * k >= HB)
             break;
-        const int hh = 2 * k + half;
+        const int hh = 4 * k + quarter;
         const float a = hh < HB ? p.A[h0 + hh] * dv[k] : 0.f;
         const float incl = warp_inclusive_scan(a);
         if (lane == 31)
             s_part[warp] = incl;
         __syncthreads();
         float before = 0.f;
-        for (int w = half * 4; w < warp; ++w)
+        for (int w = quarter * 4; w < warp; ++w)
             before += s_part[w];
         if (hh < HB) {
             sDt[hh * kRows + j] = dv[k];
@@ -209,13 +171,11 @@ __global__ void __launch_bounds__(kThreads)
         }
         __syncthreads();
     }
-    float wmax = 0.f;
     for (int i = tid; i < HB * kRows; i += kThreads) {
         const int hh = i / kRows, jj = i % kRows;
         const float last = sAcum[hh * kRows + len - 1];
         const float w = jj < len ? expf(last - sAcum[i]) * sDt[i] : 0.f;
         sWt[i] = w;
-        wmax = fmaxf(wmax, fabsf(w));
         if (jj == 0)
             p.decay[static_cast<int64_t>(blk) * p.H + h0 + hh] = expf(last);
     }
@@ -229,66 +189,31 @@ __global__ void __launch_bounds__(kThreads)
 
     const int chunks8 = NP / 8;            // 16-byte chunks per token row of x
     const int width = HB * p.P;            // valid columns
-    const int nbchunks = n_mtiles * 2 * kNBlockBytes / 16;
-    int eB = 0, eW = 0;
     if (!failed) {
-        // ---- power-of-two scales from the largest |B| and |w| * |x| ----
-        float bmax = 0.f, xmax = 0.f;
-        for (int c = tid; c < nbchunks; c += kThreads) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(sB + c * 16);
-            const __nv_bfloat16 *v = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                bmax = fmaxf(bmax, fabsf(__bfloat162float(v[k])));
-        }
-        for (int item = tid; item < kRows * chunks8; item += kThreads) {
-            const int r = item / chunks8, c0 = (item % chunks8) * 8;
-            if (r >= len || c0 >= width)
-                continue;
-            const uint32_t off = (c0 >> 6) * kNBlockBytes + (r >> 3) * 1024 + (r & 7) * 128 +
-                                 ((((c0 & 63) >> 3) ^ (r & 7)) << 4);
-            const uint4 raw = *reinterpret_cast<const uint4 *>(sW + off);
-            const __nv_bfloat16 *v = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                xmax = fmaxf(xmax, fabsf(__bfloat162float(v[k])));
-        }
-        bmax = block_max(bmax, s_red);
-        xmax = block_max(xmax, s_red);
-        wmax = block_max(wmax, s_red);
-        if (tid == 0)
-            SSD_TRACE_EV(0, 8);
-        eB = fp16_scale_exp(bmax);
-        eW = fp16_scale_exp(wmax * xmax);
-        const float sBsc = ldexpf(1.f, eB), sWsc = ldexpf(1.f, eW);
-
-        // ---- B -> fp16 in place (exact: bf16 significands fit fp16's) ----
-        for (int c = tid; c < nbchunks; c += kThreads) {
-            uint4 raw = *reinterpret_cast<const uint4 *>(sB + c * 16);
-            const __nv_bfloat16 *v = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-            uint32_t o[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                o[k] = pack_f16(__bfloat162float(v[2 * k]) * sBsc, __bfloat162float(v[2 * k + 1]) * sBsc);
-            *reinterpret_cast<uint4 *>(sB + c * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (tid == 0)
-            SSD_TRACE_EV(0, 9);
-        // ---- weighted input w_j x_j -> fp16 in place (zero past the block end) ----
+        // ---- weighted input w_j x_j split into bf16 hi (over x, in place) + lo;
+        //      zero past the block end ----
         for (int item = tid; item < kRows * chunks8; item += kThreads) {
             const int r = item / chunks8, c0 = (item % chunks8) * 8;
             const uint32_t off = (c0 >> 6) * kNBlockBytes + (r >> 3) * 1024 + (r & 7) * 128 +
                                  ((((c0 & 63) >> 3) ^ (r & 7)) << 4);
-            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
             if (r < len && c0 < width) {
                 const uint4 raw = *reinterpret_cast<const uint4 *>(sW + off);
-                const __nv_bfloat16 *v = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-                const float w = sWt[(c0 / p.P) * kRows + r] * sWsc;
+                const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                const float w = sWt[(c0 / p.P) * kRows + r];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    o[k] = pack_f16(w * __bfloat162float(v[2 * k]), w * __bfloat162float(v[2 * k + 1]));
+                for (int k = 0; k < 4; ++k) {
+                    const float2 xf = __bfloat1622float2(xb[k]);
+                    const float v0 = w * xf.x, v1 = w * xf.y;
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
+                    const float2 hf = __bfloat1622float2(h2);
+                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+                    hi[k] = *reinterpret_cast<const uint32_t *>(&h2);
+                    lo[k] = *reinterpret_cast<const uint32_t *>(&l2);
+                }
             }
-            *reinterpret_cast<uint4 *>(sW + off) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(sW + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sLo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
     }
     if (tid == 0)
@@ -302,26 +227,30 @@ __global__ void __launch_bounds__(kThreads)
         SSD_TRACE_EV(0, 4);
 
     if (tid == 0 && !failed) {
-        const uint32_t idesc = ptx::idesc_f16_f32(128, NP, 1, 1);
+        const uint32_t idesc = ptx::idesc_bf16_f32(128, NP, 1, 1);
         const uint64_t dB0 = ptx::sdesc_sw128(ptx::smem_u32(sB), kNBlockBytes, 1024);
-        const uint64_t dW0 = ptx::sdesc_sw128(ptx::smem_u32(sW), kNBlockBytes, 1024);
+        const uint64_t dH0 = ptx::sdesc_sw128(ptx::smem_u32(sW), kNBlockBytes, 1024);
+        const uint64_t dL0 = ptx::sdesc_sw128(ptx::smem_u32(sLo), kNBlockBytes, 1024);
         const int nks = (len + 15) / 16;
         for (int mt = 0; mt < n_mtiles; ++mt) {
+            const uint32_t d = tmem + mt * NP;
             const uint64_t dBm = ptx::sdesc_add(dB0, mt * 2 * kNBlockBytes);
-            ptx::mma_bf16_ss(tmem + mt * NP, dBm, dW0, idesc, 0);
-            for (int ks = 1; ks < nks; ++ks)
-                ptx::mma_bf16_ss(tmem + mt * NP, ptx::sdesc_add(dBm, ks * 2048),
-                                 ptx::sdesc_add(dW0, ks * 2048), idesc, 1);
+            ptx::mma_bf16_ss(d, dBm, dH0, idesc, 0);
+            ptx::mma_bf16_ss(d, dBm, dL0, idesc, 1);
+            for (int ks = 1; ks < nks; ++ks) {
+                const uint64_t dBk = ptx::sdesc_add(dBm, ks * 2048);
+                ptx::mma_bf16_ss(d, dBk, ptx::sdesc_add(dH0, ks * 2048), idesc, 1);
+                ptx::mma_bf16_ss(d, dBk, ptx::sdesc_add(dL0, ks * 2048), idesc, 1);
+            }
             // each state tile is stored as soon as its accumulator is final
             ptx::mma_commit(bar_mma + mt);
         }
     }
 
     if (!failed) {
-        // ---- epilogue: S^T tile [n][(h,p)] -> S_c[blk][h][p][n], scales removed ----
-        const float unscale_b = ldexpf(1.f, -eB), unscale_w = ldexpf(1.f, -eW);
-        const int q = warp & 3, chalf = warp >> 2;
-        const int ncols = NP / 2;
+        // ---- epilogue: S^T tile [n][(h,p)] -> S_c[blk][h][p][n] ----
+        const int q = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
+        const int ncols = NP / 4;
         for (int mt = 0; mt < n_mtiles && !failed; ++mt) {
             if (!ptx::mbar_wait(bar_mma + mt, 0, kWaitTimeoutNs)) {
                 failed = true;
@@ -329,27 +258,19 @@ __global__ void __launch_bounds__(kThreads)
             }
             ptx::tc_fence_after_sync();
             const int n = mt * 128 + q * 32 + lane;
-            for (int col = chalf * ncols; col < (chalf + 1) * ncols; col += 64) {
-                float v[2][32];
-                const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * NP + col;
-                ptx::tmem_ld32_pair(ta, ta + 32, v[0], v[1]);
-                if (n < p.N) {
-                    const float us = unscale_b * unscale_w;
+#pragma unroll 1
+            for (int c = cq * ncols; c < (cq + 1) * ncols; c += 16) {
+                float v[16];
+                ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * NP + c, v);
+                if (n < p.N && c < width) {
+                    // 16 columns never straddle two heads (head_dim % 16 == 0); a
+                    // warp writes 32 consecutive n of one p: 128 contiguous bytes
+                    const int hh = c / p.P, p0 = c % p.P;
+                    float *dst = p.schunk +
+                                 ((static_cast<int64_t>(blk) * p.H + h0 + hh) * p.P + p0) * p.N + n;
 #pragma unroll
-                    for (int c16 = 0; c16 < 4; ++c16) {
-                        const int c = col + c16 * 16;
-                        if (c >= width)
-                            continue;
-                        // 16 columns never straddle two heads (head_dim % 16 == 0); a
-                        // warp writes 32 consecutive n of one p: 128 contiguous bytes
-                        const int hh = c / p.P, p0 = c % p.P;
-                        float *dst = p.schunk +
-                                     ((static_cast<int64_t>(blk) * p.H + h0 + hh) * p.P + p0) * p.N + n;
-                        const float *src = &v[c16 >> 1][(c16 & 1) * 16];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            dst[static_cast<int64_t>(k) * p.N] = src[k] * us;
-                    }
+                    for (int k = 0; k < 16; ++k)
+                        dst[static_cast<int64_t>(k) * p.N] = v[k];
                 }
             }
         }
@@ -376,13 +297,14 @@ K1Config chunk_state_config(int H, int G, int P, int N)
     K1Config c{};
     const int hpg = H / G;
     c.n_mtiles = (N + 127) / 128;
-    // heads per CTA: columns of one MMA (<= 128, so that two CTAs share an SM's
-    // tensor memory and shared memory), at most 8 heads
+    // heads per CTA: as many as one MMA's columns hold (<= 256; the tensor
+    // core is most efficient at N = 256 and B is shared), at most 8 heads
+    // (the dt prologue holds 2 per thread)
     for (int hb = hpg < 8 ? hpg : 8; hb >= 1; --hb) {
         if (hpg % hb)
             continue;
         const int np = pad64(hb * P);
-        if (np > 128 && hb > 1)
+        if ((np > 256 || c.n_mtiles * np > 512) && hb > 1)
             continue;
         c.HB = hb;
         c.NP = np;
