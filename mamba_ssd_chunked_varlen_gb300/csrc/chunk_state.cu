@@ -94,6 +94,11 @@ __global__ void __launch_bounds__(kThreads)
     if (tid == 0)
         SSD_TRACE_EV(0, 0);
 
+    if (tid == 0) {
+        // descriptors fetched while the block is being mapped
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmX);
+    }
     if (leader && tid == 0)
         p.hdr->errors = 0u;
     const BlockInfo bi = map_block<kThreads>(p, blk, scratch, leader ? p.seq_first : nullptr);
@@ -146,19 +151,19 @@ __global__ void __launch_bounds__(kThreads)
     // ---- dt, softplus, cumulative A*dt per head: every head's dt loaded at
     //      once (one round trip), then four heads per scan pass ----
     const int quarter = tid >> 7, j = tid & 127;
-    float dv[2];
+    float dv[2], av[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int hh = 4 * k + quarter;
         dv[k] = (hh < HB && j < len) ? processed_dt(p, t0 + j, h0 + hh) : 0.f;
+        av[k] = hh < HB ? p.A[h0 + hh] : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         if (4 * k >= HB)
             break;
         const int hh = 4 * k + quarter;
-        const float a = hh < HB ? p.A[h0 + hh] * dv[k] : 0.f;
-        const float incl = warp_inclusive_scan(a);
+        const float incl = warp_inclusive_scan(av[k] * dv[k]);
         if (lane == 31)
             s_part[warp] = incl;
         __syncthreads();

@@ -44,7 +44,8 @@ struct ChunkScanMaps {
 struct K3Config {
     int HB;          // heads per CTA (one group)
     int P_pad, N_pad;
-    int nS, nX, nY;  // ring depths: S_prev tiles, X tiles, TMEM accumulator slots
+    int n_xb;        // 64-column X blocks a CTA loads (its heads, from a 64-aligned start)
+    int YG;          // heads per off-diagonal MMA (their S_prev tiles stacked along N)
     size_t smem;
 };
 K3Config chunk_scan_config(int H, int G, int P, int N);

@@ -81,7 +81,7 @@ def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row(pkg):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(pkg):
-    w = W.make_workload("big", [3000, 3000, 3000], 16, 64, 1, 256, 256, max_slots=3, seed=5)
+    w = W.make_workload("big", [4200, 4200, 4200, 4200], 16, 64, 1, 256, 256, max_slots=4, seed=5)
     need = pkg.ssd_scan_varlen_workspace_size(w.total_len, w.batch, w.nheads, w.head_dim,
                                               w.ngroups, w.dstate, w.chunk_size)
     assert need > pkg.binding.NOALLOC_SCRATCH_BYTES
