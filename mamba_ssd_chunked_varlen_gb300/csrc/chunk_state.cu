@@ -90,7 +90,11 @@ __global__ void __launch_bounds__(kThreads)
     const int blk = blockIdx.x;
     const int h0 = blockIdx.y * HB;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool leader = blockIdx.x == 0 && blockIdx.y == 0;
+    // The per-call bookkeeping (block table, error word, slot checks) falls to
+    // CTA (max_chunks - 1, 0): the number of blocks is sum_b ceil(L_b / Q) <
+    // T / Q + batch <= max_chunks, so that CTA never holds a block and the
+    // bookkeeping delays no block's work.
+    const bool leader = blockIdx.x == gridDim.x - 1 && blockIdx.y == 0;
     if (tid == 0)
         SSD_TRACE_EV(0, 0);
 
