@@ -271,8 +271,20 @@ def run_ours(args, rank, world, local):
                              w.chunk_size, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
+    if args.form == "states":
+        # the separate-state-array form: initial_states are the workload's pool
+        # rows of its sequences, final_states a (batch, H, P, N) output
+        init_states = d["pool"][d["cidx"].long()].contiguous()
+        final_states = torch.empty_like(init_states)
+
     def call(yy=None, dd=None):
         dd = d if dd is None else dd
+        if args.form == "states":
+            pkg.ssd_scan_varlen_fwd_states(
+                yy if yy is not None else y, dd["x"], dd["dt"], d["A"], dd["B"], dd["C"], d["D"],
+                d["dt_bias"], init_states, dd["hinit"], final_states, dd["qsl"],
+                chunk_size=w.chunk_size, dt_softplus=w.dt_softplus, workspace=ws, stream=stream)
+            return
         pkg.ssd_scan_varlen_fwd(yy if yy is not None else y, dd["x"], dd["dt"], d["A"], dd["B"],
                                 dd["C"], d["D"], d["dt_bias"], d["pool"], dd["qsl"],
                                 dd["hinit"], dd["cidx"], chunk_size=w.chunk_size,
@@ -383,7 +395,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded; shapes and value recipe of the workload)",
         "config": {"workload": w.name, "total_len": T, "batch": w.batch, "nheads": w.nheads,
                    "head_dim": w.head_dim, "ngroups": w.ngroups, "dstate": w.dstate,
-                   "chunk_size": w.chunk_size, "chunks": model["chunks"],
+                   "chunk_size": w.chunk_size, "chunks": model["chunks"], "form": args.form,
                    "l2": f"flushed before every timed call ({L2_FLUSH_BYTES >> 20} MB write)",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": round(mean_ms_all * 1e3, 3),
@@ -479,6 +491,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="kernelindex", choices=W.WORKLOADS)
+    ap.add_argument("--form", choices=("inplace", "states"), default="inplace",
+                    help="inplace: ssd_scan_varlen_fwd (slot pool); states: "
+                         "ssd_scan_varlen_fwd_states (separate initial/final state arrays); "
+                         "the per-stage attribution always uses the in-place profiled call")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

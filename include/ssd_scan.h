@@ -118,6 +118,35 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd(
     int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
     void *workspace, size_t workspace_bytes, ssd_stream_t stream);
 
+/* The same scan with separate state arrays instead of the slot pool: the form
+ * of the "mamba2_ssd_scan" module description, whose state "resets to zero (or
+ * to initial_states)" at each sequence start and whose final_states
+ * (batch, nheads, head_dim, dstate) is "written at each sequence end"; the
+ * in-place op of "Mamba2SSDChunkScanVarlenFwdInplace" differs only in reading
+ * and writing these through ssm_pool[cache_indices[b]].
+ *
+ *   initial_states    fp32 (batch, nheads, head_dim, dstate) or NULL (zero
+ *                     initial states); 16-byte aligned
+ *   has_initial_state uint8 (batch) or NULL; when given, sequence b starts
+ *                     from initial_states[b] only if has_initial_state[b] is
+ *                     nonzero (zero otherwise); when NULL every sequence starts
+ *                     from initial_states[b] (or zero if that is NULL)
+ *   final_states      fp32 (batch, nheads, head_dim, dstate) out, 16-byte
+ *                     aligned; row b written for every sequence, also of
+ *                     length 0 (with its initial state); may alias
+ *                     initial_states (each element is read before it is written)
+ *
+ * Every other argument, the workspace size, the supported sizes and the errors
+ * are those of ssd_scan_varlen_fwd (NULL final_states with batch > 0:
+ * SSD_ERR_INVALID_ARG). */
+SSD_API ssd_status_t ssd_scan_varlen_fwd_states(
+    void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, const float *dt_bias, const float *initial_states,
+    const uint8_t *has_initial_state, float *final_states, const int32_t *query_start_loc,
+    int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups,
+    int32_t dstate, int32_t chunk_size, int32_t dt_softplus, void *workspace,
+    size_t workspace_bytes, ssd_stream_t stream);
+
 /* ssd_scan_varlen_fwd with per-stage timing: `events` points to 4 CUDA events
  * (cudaEvent_t, created by the caller) that are recorded on `stream` before
  * the first stage and after each of the three launches (chunk state, state

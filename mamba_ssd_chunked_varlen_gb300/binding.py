@@ -19,6 +19,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_workspace_size",
     "ssd_scan_varlen_fwd",
     "ssd_scan_varlen_fwd_profiled",
+    "ssd_scan_varlen_fwd_states",
     "ssd_scan_varlen_fwd_noalloc",
     "ssd_scan_varlen_read_errors",
     "ssd_status_string",
@@ -58,6 +59,9 @@ def library() -> ctypes.CDLL:
                                         + [vp, sz, vp])
     lib.ssd_scan_varlen_fwd_profiled.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_profiled.argtypes = lib.ssd_scan_varlen_fwd.argtypes + [vp]
+    lib.ssd_scan_varlen_fwd_states.restype = ctypes.c_int
+    lib.ssd_scan_varlen_fwd_states.argtypes = ([vp] * 12 + [i64, i32, i32, i32, i32, i32, i32, i32]
+                                               + [vp, sz, vp])
     lib.ssd_scan_varlen_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_noalloc.argtypes = lib.ssd_scan_varlen_fwd.argtypes[:21] + [vp]
     lib.ssd_scan_varlen_read_errors.restype = ctypes.c_int
@@ -166,6 +170,41 @@ def ssd_scan_varlen_fwd(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc
                    cache_indices, chunk_size, dt_softplus, workspace, stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_scan_varlen_fwd")
+
+
+def ssd_scan_varlen_fwd_states(y, x, dt, A, B, C, D, dt_bias, initial_states,
+                               has_initial_state, final_states, query_start_loc, *,
+                               chunk_size: int, dt_softplus: bool = True, workspace=None,
+                               stream=None) -> None:
+    """The scan with separate state arrays instead of the slot pool:
+    initial_states (batch, H, P, N) fp32 or None (zero initial states),
+    has_initial_state (batch,) uint8/bool or None (None: every sequence starts
+    from initial_states), final_states (batch, H, P, N) fp32 written for every
+    sequence.  Other arguments as ssd_scan_varlen_fwd."""
+    import torch
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    batch = query_start_loc.shape[0] - 1
+    if workspace is None:
+        raise ValueError("workspace is required (see ssd_scan_varlen_workspace_size)")
+    if has_initial_state is not None and has_initial_state.dtype == torch.bool:
+        has_initial_state = has_initial_state.view(torch.uint8)
+    for name, t in (("initial_states", initial_states), ("final_states", final_states)):
+        if t is not None and tuple(t.shape) != (batch, H, P, N):
+            raise ValueError(f"{name} must have shape {(batch, H, P, N)}")
+    st = library().ssd_scan_varlen_fwd_states(
+        _ptr(y, "y", torch.bfloat16), _ptr(x, "x", torch.bfloat16),
+        _ptr(dt, "dt", torch.bfloat16), _ptr(A, "A", torch.float32),
+        _ptr(B, "B", torch.bfloat16), _ptr(C, "C", torch.bfloat16),
+        _ptr(D, "D", torch.float32, True), _ptr(dt_bias, "dt_bias", torch.float32, True),
+        _ptr(initial_states, "initial_states", torch.float32, True),
+        _ptr(has_initial_state, "has_initial_state", torch.uint8, True),
+        _ptr(final_states, "final_states", torch.float32),
+        _ptr(query_start_loc, "query_start_loc", torch.int32),
+        T, batch, H, P, G, N, int(chunk_size), int(bool(dt_softplus)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan_varlen_fwd_states")
 
 
 def ssd_scan_varlen_fwd_noalloc(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,

@@ -119,11 +119,10 @@ int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
 namespace ssd {
 
 ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
-                       const void *C, const float *D, const float *dt_bias, float *ssm_pool,
+                       const void *C, const float *D, const float *dt_bias, const StateIO &io,
                        const int32_t *query_start_loc, const uint8_t *has_initial_state,
-                       const uint32_t *cache_indices, int64_t total_len, int32_t batch,
-                       int32_t nheads, int32_t head_dim, int32_t ngroups, int32_t dstate,
-                       int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+                       int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim,
+                       int32_t ngroups, int32_t dstate, int32_t chunk_size, int32_t dt_softplus,
                        void *workspace, size_t workspace_bytes, ssd_stream_t stream_,
                        void *const *events)
 {
@@ -131,17 +130,20 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
         check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size);
     if (sz != SSD_OK)
         return sz;
-    if (max_slots < 0)
+    const bool in_place = io.pool != nullptr;
+    if (in_place && io.max_slots < 0)
         return SSD_ERR_INVALID_ARG;
     if (batch == 0)
         return SSD_OK;
-    if (!query_start_loc || !cache_indices || !ssm_pool || !A)
+    if (!query_start_loc || !A)
+        return SSD_ERR_INVALID_ARG;
+    if (in_place ? !io.cache_indices : !io.final_states)
         return SSD_ERR_INVALID_ARG;
     if (total_len > 0 && (!y || !x || !dt || !B || !C))
         return SSD_ERR_INVALID_ARG;
     if (total_len > 0 && (!aligned16(y) || !aligned16(x) || !aligned16(B) || !aligned16(C)))
         return SSD_ERR_INVALID_ARG;
-    if (!aligned16(ssm_pool))
+    if (!aligned16(io.pool) || !aligned16(io.initial_states) || !aligned16(io.final_states))
         return SSD_ERR_INVALID_ARG;
     const int32_t Qb = ssd::block_tokens(chunk_size);
     const ssd::WsLayout L = ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, Qb);
@@ -161,10 +163,13 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.A = A;
     p.D = D;
     p.dt_bias = dt_bias;
-    p.pool = ssm_pool;
+    p.pool = io.pool;
+    p.cache_idx = io.cache_indices;
+    p.max_slots = io.max_slots;
+    p.init_states = io.initial_states;
+    p.final_states = io.final_states;
     p.qsl = query_start_loc;
     p.has_init = has_initial_state;
-    p.cache_idx = cache_indices;
     p.T = total_len;
     p.batch = batch;
     p.H = nheads;
@@ -172,7 +177,6 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.G = ngroups;
     p.N = dstate;
     p.Q = Qb;
-    p.max_slots = max_slots;
     p.dt_softplus = dt_softplus ? 1 : 0;
     p.max_chunks = static_cast<int32_t>(L.max_chunks);
     p.hdr = reinterpret_cast<ssd::WsHeader *>(ws + L.header);
@@ -231,9 +235,28 @@ ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const f
                                  int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
                                  void *workspace, size_t workspace_bytes, ssd_stream_t stream)
 {
-    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
-                     cache_indices, total_len, batch, nheads, head_dim, ngroups, dstate, max_slots,
-                     chunk_size, dt_softplus, workspace, workspace_bytes, stream, nullptr);
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    if (!ssm_pool && batch > 0)
+        return SSD_ERR_INVALID_ARG;
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
+                          total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
+                          dt_softplus, workspace, workspace_bytes, stream, nullptr);
+}
+
+ssd_status_t ssd_scan_varlen_fwd_states(void *y, const void *x, const void *dt, const float *A,
+                                        const void *B, const void *C, const float *D,
+                                        const float *dt_bias, const float *initial_states,
+                                        const uint8_t *has_initial_state, float *final_states,
+                                        const int32_t *query_start_loc, int64_t total_len,
+                                        int32_t batch, int32_t nheads, int32_t head_dim,
+                                        int32_t ngroups, int32_t dstate, int32_t chunk_size,
+                                        int32_t dt_softplus, void *workspace,
+                                        size_t workspace_bytes, ssd_stream_t stream)
+{
+    const ssd::StateIO io{nullptr, nullptr, 0, initial_states, final_states};
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
+                          total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
+                          dt_softplus, workspace, workspace_bytes, stream, nullptr);
 }
 
 ssd_status_t ssd_scan_varlen_fwd_profiled(
@@ -249,9 +272,12 @@ ssd_status_t ssd_scan_varlen_fwd_profiled(
     for (int k = 0; k < 4; ++k)
         if (!events[k])
             return SSD_ERR_INVALID_ARG;
-    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
-                     cache_indices, total_len, batch, nheads, head_dim, ngroups, dstate, max_slots,
-                     chunk_size, dt_softplus, workspace, workspace_bytes, stream, events);
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    if (!ssm_pool && batch > 0)
+        return SSD_ERR_INVALID_ARG;
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
+                          total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
+                          dt_softplus, workspace, workspace_bytes, stream, events);
 }
 
 ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stream_t stream_,

@@ -180,10 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t0 = bi.t0, len = bi.len;
     const int g = h0 / (p.H / p.G);
     const int nkb = N_pad / 64;
-    const uint32_t slot_idx = p.cache_idx[bi.seq];
     // the state entering the block is zero for a first block without initial state
-    const bool has_prev = !bi.first || (p.has_init != nullptr && p.has_init[bi.seq] != 0 &&
-                                        static_cast<int64_t>(slot_idx) < p.max_slots);
+    const bool has_prev = !bi.first || seq_init_state(p, bi.seq) != nullptr;
     // X columns of the CTA's heads, loaded from a 64-aligned start
     const int x_base = (h0 * p.P / 64) * 64;
     const int n_xb = ((h0 + HB) * p.P - x_base + 63) / 64;

@@ -107,9 +107,10 @@ __global__ void __launch_bounds__(kThreads)
         p.hdr->errors = 0u;
     const BlockInfo bi = map_block<kThreads>(p, blk, scratch, leader ? p.seq_first : nullptr);
     if (leader) {
-        for (int b = tid; b < p.batch; b += kThreads)
-            if (static_cast<int64_t>(p.cache_idx[b]) >= p.max_slots)
-                record_error(p.hdr, kErrBadSlot);
+        if (p.pool != nullptr)
+            for (int b = tid; b < p.batch; b += kThreads)
+                if (static_cast<int64_t>(p.cache_idx[b]) >= p.max_slots)
+                    record_error(p.hdr, kErrBadSlot);
         if (tid == 0) {
             if (!bi.valid)
                 record_error(p.hdr, kErrBadQsl);

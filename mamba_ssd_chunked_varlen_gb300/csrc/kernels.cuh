@@ -52,14 +52,24 @@ K3Config chunk_scan_config(int H, int G, int P, int N);
 cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps, cudaStream_t stream,
                               bool programmatic);
 
-// The whole scan (argument checks, tensor maps, the four launches) on a
-// caller-provided scratch buffer; `events` (5 CUDA events) may be null.
+// Where the sequences' states start and end: the slot pool (in place, as
+// "Mamba2SSDChunkScanVarlenFwdInplace") when pool is set, else separate
+// per-sequence arrays (the final_states form of "mamba2_ssd_scan").
+struct StateIO {
+    float *pool;                  // (max_slots, H, P, N) or null
+    const uint32_t *cache_indices;
+    int64_t max_slots;
+    const float *initial_states;  // (batch, H, P, N) or null (zero initial states)
+    float *final_states;          // (batch, H, P, N)
+};
+
+// The whole scan (argument checks, tensor maps, the three launches) on a
+// caller-provided scratch buffer; `events` (4 CUDA events) may be null.
 ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
-                       const void *C, const float *D, const float *dt_bias, float *ssm_pool,
+                       const void *C, const float *D, const float *dt_bias, const StateIO &io,
                        const int32_t *query_start_loc, const uint8_t *has_initial_state,
-                       const uint32_t *cache_indices, int64_t total_len, int32_t batch,
-                       int32_t nheads, int32_t head_dim, int32_t ngroups, int32_t dstate,
-                       int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+                       int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim,
+                       int32_t ngroups, int32_t dstate, int32_t chunk_size, int32_t dt_softplus,
                        void *workspace, size_t workspace_bytes, ssd_stream_t stream,
                        void *const *events);
 

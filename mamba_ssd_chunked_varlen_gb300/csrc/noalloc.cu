@@ -55,11 +55,13 @@ extern "C" ssd_status_t ssd_scan_varlen_fwd_noalloc(
 {
     const size_t need = ssd_scan_varlen_workspace_size(total_len, batch, nheads, head_dim,
                                                        ngroups, dstate, chunk_size);
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    if (!ssm_pool && batch > 0)
+        return SSD_ERR_INVALID_ARG;
     if (need == 0)  // invalid or unsupported sizes: let the full check name the reason
-        return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
-                              has_initial_state, cache_indices, total_len, batch, nheads,
-                              head_dim, ngroups, dstate, max_slots, chunk_size, dt_softplus,
-                              nullptr, 0, stream, nullptr);
+        return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc,
+                              has_initial_state, total_len, batch, nheads, head_dim, ngroups,
+                              dstate, chunk_size, dt_softplus, nullptr, 0, stream, nullptr);
     if (need > SSD_NOALLOC_SCRATCH_BYTES)
         return SSD_ERR_TOO_LARGE;
     if (batch == 0)
@@ -67,8 +69,7 @@ extern "C" ssd_status_t ssd_scan_varlen_fwd_noalloc(
     void *scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess)
         return SSD_ERR_CUDA;
-    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
-                          has_initial_state, cache_indices, total_len, batch, nheads, head_dim,
-                          ngroups, dstate, max_slots, chunk_size, dt_softplus, scratch,
-                          SSD_NOALLOC_SCRATCH_BYTES, stream, nullptr);
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
+                          total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
+                          dt_softplus, scratch, SSD_NOALLOC_SCRATCH_BYTES, stream, nullptr);
 }

@@ -77,10 +77,15 @@ struct ScanParams {
     const float *A;
     const float *D;        // may be null
     const float *dt_bias;  // may be null
+    // where each sequence's state starts and ends: either the slot pool
+    // (in place: pool, cache_idx, max_slots) or, when pool is null, separate
+    // per-sequence arrays (init_states may be null: zero initial states)
     float *pool;
+    const uint32_t *cache_idx;
+    const float *init_states;  // (batch, H, P, N) or null
+    float *final_states;       // (batch, H, P, N)
     const int32_t *qsl;
     const uint8_t *has_init;  // may be null
-    const uint32_t *cache_idx;
     int64_t T;
     int32_t batch, H, P, G, N;
     int32_t Q;            // tokens per block (block_tokens of the chunk size)

@@ -59,6 +59,38 @@ __device__ __forceinline__ T warp_inclusive_scan(T v)
     return v;
 }
 
+// ---------------------------------------------------------------- state I/O
+// Sequence b's initial state (null: zero).  In place ("Mamba2SSDChunkScanVarlen
+// FwdInplace"): its pool slot when has_initial_state[b] is set and the slot
+// index is in range.  Separate arrays (the "mamba2_ssd_scan" final_states
+// form): initial_states[b] unless has_initial_state is given and false.
+__device__ __forceinline__ const float *seq_init_state(const ScanParams &p, int b)
+{
+    const int64_t slot_elems = static_cast<int64_t>(p.H) * p.P * p.N;
+    const bool flag = p.has_init == nullptr || p.has_init[b] != 0;
+    if (p.pool != nullptr) {
+        const uint32_t slot = p.cache_idx[b];
+        return (p.has_init != nullptr && flag && static_cast<int64_t>(slot) < p.max_slots)
+                   ? p.pool + static_cast<int64_t>(slot) * slot_elems
+                   : nullptr;
+    }
+    return (p.init_states != nullptr && flag) ? p.init_states + static_cast<int64_t>(b) * slot_elems
+                                              : nullptr;
+}
+
+// Where sequence b's final state goes (null: nowhere, an out-of-range slot).
+__device__ __forceinline__ float *seq_final_state(const ScanParams &p, int b)
+{
+    const int64_t slot_elems = static_cast<int64_t>(p.H) * p.P * p.N;
+    if (p.pool != nullptr) {
+        const uint32_t slot = p.cache_idx[b];
+        return static_cast<int64_t>(slot) < p.max_slots
+                   ? p.pool + static_cast<int64_t>(slot) * slot_elems
+                   : nullptr;
+    }
+    return p.final_states + static_cast<int64_t>(b) * slot_elems;
+}
+
 // ---------------------------------------------------------------- block map
 // Where a block (at most `blk_len` tokens of one sequence, aligned to the
 // sequence start) lies: blocks are numbered sequence after sequence.

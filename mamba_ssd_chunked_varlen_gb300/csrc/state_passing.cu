@@ -6,6 +6,8 @@
 //   for each block c of b:  S_prev[c] = S;   S = decay_c * S + S_c[c]
 //   ssm_pool[slot][h] = S                      (in-place write-back, page
 //                                               "Mamba2SSDChunkScanVarlenFwdInplace")
+// or, in the form with separate state arrays, S starts from initial_states[b]
+// and ends in final_states[b] (the "mamba2_ssd_scan" module description).
 //
 // Every (p, n) element is an independent chain, so the grid covers the
 // head_dim x dstate elements of every (sequence, head) with 4 elements per
@@ -41,14 +43,13 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(ScanParams p, i
     if (b >= p.batch || e >= PN)
         return;
 
-    const uint32_t slot = p.cache_idx[b];
-    const bool slot_ok = static_cast<int64_t>(slot) < p.max_slots;
-    const bool init = slot_ok && p.has_init != nullptr && p.has_init[b] != 0;
-    float *pool_h = p.pool + (static_cast<int64_t>(slot) * p.H + h) * PN + e;
+    const float *init = seq_init_state(p, b);
+    float *fin = seq_final_state(p, b);
+    const int64_t off = static_cast<int64_t>(h) * PN + e;
 
     float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
     if (init)
-        S = *reinterpret_cast<const float4 *>(pool_h);
+        S = *reinterpret_cast<const float4 *>(init + off);
 
     const int c_begin = p.seq_first[b], c_end = p.seq_first[b + 1];
     const int64_t stride = static_cast<int64_t>(p.H) * PN;
@@ -82,8 +83,8 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(ScanParams p, i
         sp += kAhead * stride;
         dec += static_cast<int64_t>(kAhead) * p.H;
     }
-    if (slot_ok)
-        *reinterpret_cast<float4 *>(pool_h) = S;
+    if (fin)
+        *reinterpret_cast<float4 *>(fin + off) = S;
     if (threadIdx.x == 0)
         SSD_TRACE_EV(1, 2);
 }

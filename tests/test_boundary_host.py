@@ -94,3 +94,27 @@ def test_host_checks_reject_before_any_launch(lib):
     assert _call(lib, ws=(1 << 12) + 16) == 3      # workspace alignment
     assert _call(lib, T=-1) == 1
     assert _call(lib, batch=0, x=None, y=None) == 0  # empty batch: nothing to do
+
+
+def _call_states(lib, **over):
+    args = dict(y=1 << 12, x=1 << 12, dt=1 << 12, A=1 << 12, B=1 << 12, C=1 << 12, D=None,
+                dt_bias=None, init=None, hinit=None, final=1 << 12, qsl=1 << 12,
+                T=512, batch=1, H=4, P=32, G=1, N=32, Q=64, sp=1, ws=1 << 12, wsb=1 << 30)
+    args.update(over)
+    vp = lambda v: None if v is None else ctypes.c_void_p(v)
+    return lib.ssd_scan_varlen_fwd_states(
+        vp(args["y"]), vp(args["x"]), vp(args["dt"]), vp(args["A"]), vp(args["B"]),
+        vp(args["C"]), vp(args["D"]), vp(args["dt_bias"]), vp(args["init"]), vp(args["hinit"]),
+        vp(args["final"]), vp(args["qsl"]), args["T"], args["batch"], args["H"], args["P"],
+        args["G"], args["N"], args["Q"], args["sp"], vp(args["ws"]), args["wsb"], None)
+
+
+def test_states_form_host_checks(lib):
+    # The separate-state-array form shares the in-place form's checks, plus its own.
+    assert _call_states(lib, final=None) == 1          # final_states required
+    assert _call_states(lib, final=(1 << 12) + 8) == 1  # final_states 16-byte aligned
+    assert _call_states(lib, init=(1 << 12) + 4) == 1   # initial_states 16-byte aligned
+    assert _call_states(lib, qsl=None) == 1
+    assert _call_states(lib, N=512) == 2
+    assert _call_states(lib, ws=None) == 3
+    assert _call_states(lib, batch=0, final=None) == 0  # empty batch: nothing to do
