@@ -199,31 +199,66 @@ __global__ void __launch_bounds__(kThreads)
 
     const int chunks8 = NP / 8;            // 16-byte chunks per token row of x
     const int width = HB * p.P;            // valid columns
-    if (!failed) {
-        // ---- weighted input w_j x_j split into bf16 hi (over x, in place) + lo;
-        //      zero past the block end ----
-        for (int item = tid; item < kRows * chunks8; item += kThreads) {
-            const int r = item / chunks8, c0 = (item % chunks8) * 8;
-            const uint32_t off = (c0 >> 6) * kNBlockBytes + (r >> 3) * 1024 + (r & 7) * 128 +
-                                 ((((c0 & 63) >> 3) ^ (r & 7)) << 4);
-            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
-            if (r < len && c0 < width) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(sW + off);
-                const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-                const float w = sWt[(c0 / p.P) * kRows + r];
+    const int log2P = __ffs(p.P) - 1;
+    // weighted input w_j x_j of one 16-byte chunk (8 columns) of row r, split
+    // into bf16 hi + lo; zero past the block end and past the CTA's heads
+    auto hilo = [&](const uint4 &raw, int r, int c0, uint4 &hi4, uint4 &lo4) {
+        uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+        if (r < len && c0 < width) {
+            const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+            const float w = sWt[(c0 >> log2P) * kRows + r];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 xf = __bfloat1622float2(xb[k]);
-                    const float v0 = w * xf.x, v1 = w * xf.y;
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
-                    const float2 hf = __bfloat1622float2(h2);
-                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
-                    hi[k] = *reinterpret_cast<const uint32_t *>(&h2);
-                    lo[k] = *reinterpret_cast<const uint32_t *>(&l2);
-                }
+            for (int k = 0; k < 4; ++k) {
+                const float2 xf = __bfloat1622float2(xb[k]);
+                const float v0 = w * xf.x, v1 = w * xf.y;
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
+                const float2 hf = __bfloat1622float2(h2);
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+                hi[k] = *reinterpret_cast<const uint32_t *>(&h2);
+                lo[k] = *reinterpret_cast<const uint32_t *>(&l2);
             }
-            *reinterpret_cast<uint4 *>(sW + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(sLo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        hi4 = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        lo4 = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    };
+    auto swz = [&](int r, int c0) -> uint32_t {
+        return (c0 >> 6) * kNBlockBytes + (r >> 3) * 1024 + (r & 7) * 128 +
+               ((((c0 & 63) >> 3) ^ (r & 7)) << 4);
+    };
+    if (!failed) {
+        // ---- the weighted operand, hi over x in place, lo beside it ----
+        if ((chunks8 & (chunks8 - 1)) == 0) {
+            // each thread keeps one column chunk and takes rows r0, r0 + rstep, ...;
+            // four rows are loaded before any of them is rewritten
+            const int lc = __ffs(chunks8) - 1;
+            const int c0 = (tid & (chunks8 - 1)) * 8;
+            const int rstep = kThreads >> lc;
+#pragma unroll 1
+            for (int r0 = tid >> lc; r0 < kRows; r0 += 4 * rstep) {
+                uint4 raw[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (r0 + k * rstep < kRows)
+                        raw[k] = *reinterpret_cast<const uint4 *>(sW + swz(r0 + k * rstep, c0));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (r0 + k * rstep < kRows) {
+                        const int r = r0 + k * rstep;
+                        uint4 hi4, lo4;
+                        hilo(raw[k], r, c0, hi4, lo4);
+                        *reinterpret_cast<uint4 *>(sW + swz(r, c0)) = hi4;
+                        *reinterpret_cast<uint4 *>(sLo + swz(r, c0)) = lo4;
+                    }
+            }
+        } else {
+            for (int item = tid; item < kRows * chunks8; item += kThreads) {
+                const int r = item / chunks8, c0 = (item % chunks8) * 8;
+                const uint4 raw = *reinterpret_cast<const uint4 *>(sW + swz(r, c0));
+                uint4 hi4, lo4;
+                hilo(raw, r, c0, hi4, lo4);
+                *reinterpret_cast<uint4 *>(sW + swz(r, c0)) = hi4;
+                *reinterpret_cast<uint4 *>(sLo + swz(r, c0)) = lo4;
+            }
         }
     }
     if (tid == 0)

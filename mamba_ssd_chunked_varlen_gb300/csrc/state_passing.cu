@@ -25,7 +25,9 @@ constexpr int kThreads = 256;
 constexpr int kVec = 4;
 constexpr int kAhead = 8;  // blocks loaded ahead of use
 
-__global__ void __launch_bounds__(kThreads) state_passing_kernel(ScanParams p, int blocks_per_head)
+// at most 64 registers: two of these CTAs fit beside a chunk-state CTA on an
+// SM while they wait for it
+__global__ void __launch_bounds__(kThreads, 4) state_passing_kernel(ScanParams p, int blocks_per_head)
 {
     if (threadIdx.x == 0)
         SSD_TRACE_EV(1, 0);
