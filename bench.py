@@ -276,9 +276,31 @@ def run_ours(args, rank, world, local):
         # rows of its sequences, final_states a (batch, H, P, N) output
         init_states = d["pool"][d["cidx"].long()].contiguous()
         final_states = torch.empty_like(init_states)
+    if args.form == "strided":
+        # x, B, C, dt as column slices of one fused projection output
+        # [x | B | C | dt | pad] per token (y stays contiguous)
+        H_, P_, G_, N_ = w.nheads, w.head_dim, w.ngroups, w.dstate
+        o_b = H_ * P_
+        o_c = o_b + G_ * N_
+        o_dt = o_c + G_ * N_
+        width = (o_dt + H_ + 7) // 8 * 8
+        fused = torch.zeros((T, width), dtype=torch.bfloat16, device=dev)
+        fused[:, :o_b] = d["x"].reshape(T, -1)
+        fused[:, o_b:o_c] = d["B"].reshape(T, -1)
+        fused[:, o_c:o_dt] = d["C"].reshape(T, -1)
+        fused[:, o_dt:o_dt + H_] = d["dt"]
+        sv = {"x": fused[:, :o_b].unflatten(1, (H_, P_)),
+              "B": fused[:, o_b:o_c].unflatten(1, (G_, N_)),
+              "C": fused[:, o_c:o_dt].unflatten(1, (G_, N_)), "dt": fused[:, o_dt:o_dt + H_]}
 
     def call(yy=None, dd=None):
         dd = d if dd is None else dd
+        if args.form == "strided" and dd is d:
+            pkg.ssd_scan_varlen_fwd_strided(
+                yy if yy is not None else y, sv["x"], sv["dt"], d["A"], sv["B"], sv["C"], d["D"],
+                d["dt_bias"], d["pool"], d["qsl"], d["hinit"], d["cidx"], chunk_size=w.chunk_size,
+                dt_softplus=w.dt_softplus, workspace=ws, stream=stream)
+            return
         if args.form == "states":
             pkg.ssd_scan_varlen_fwd_states(
                 yy if yy is not None else y, dd["x"], dd["dt"], d["A"], dd["B"], dd["C"], d["D"],
@@ -491,9 +513,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="kernelindex", choices=W.WORKLOADS)
-    ap.add_argument("--form", choices=("inplace", "states"), default="inplace",
+    ap.add_argument("--form", choices=("inplace", "states", "strided"), default="inplace",
                     help="inplace: ssd_scan_varlen_fwd (slot pool); states: "
                          "ssd_scan_varlen_fwd_states (separate initial/final state arrays); "
+                         "strided: ssd_scan_varlen_fwd_strided on x, B, C, dt cut from one "
+                         "fused projection buffer (the e2e leg copies contiguous inputs); "
                          "the per-stage attribution always uses the in-place profiled call")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")

@@ -118,6 +118,31 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd(
     int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
     void *workspace, size_t workspace_bytes, ssd_stream_t stream);
 
+/* Elements (not bytes) between consecutive tokens of each token-major input
+ * and of y; 0 means contiguous (H*P for x and y, H for dt, G*N for B and C).
+ * Within a token, x / y rows stay (H, P) contiguous, B / C rows (G, N) and dt
+ * (H).  This is the layout of column slices of one wider buffer, e.g. x, B, C
+ * and dt cut from a fused projection output (the per-tensor stride metadata
+ * of the "mamba2_ssd_scan" comptime values Strides1D..Strides4D). */
+typedef struct {
+    int64_t x, dt, B, C, y;
+} ssd_token_strides_t;
+
+/* ssd_scan_varlen_fwd on strided token-major tensors.  Each nonzero stride
+ * must be at least the contiguous one; the strides of x, B, C and y must be
+ * multiples of 8 elements (16 bytes: TMA row pitch, 16-byte y stores), else
+ * SSD_ERR_INVALID_ARG.  dt's stride is free.  strides == NULL is
+ * ssd_scan_varlen_fwd.  Other arguments, results and errors as
+ * ssd_scan_varlen_fwd. */
+SSD_API ssd_status_t ssd_scan_varlen_fwd_strided(
+    void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, const float *dt_bias, float *ssm_pool, const int32_t *query_start_loc,
+    const uint8_t *has_initial_state, const uint32_t *cache_indices,
+    int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups,
+    int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+    const ssd_token_strides_t *strides, void *workspace, size_t workspace_bytes,
+    ssd_stream_t stream);
+
 /* The same scan with separate state arrays instead of the slot pool: the form
  * of the "mamba2_ssd_scan" module description, whose state "resets to zero (or
  * to initial_states)" at each sequence start and whose final_states

@@ -20,6 +20,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_fwd",
     "ssd_scan_varlen_fwd_profiled",
     "ssd_scan_varlen_fwd_states",
+    "ssd_scan_varlen_fwd_strided",
     "ssd_scan_varlen_fwd_noalloc",
     "ssd_scan_varlen_read_errors",
     "ssd_status_string",
@@ -34,6 +35,12 @@ DEVERR_BAD_CACHE_INDEX = 0x2
 DEVERR_TIMEOUT = 0x4
 
 _lib: Optional[ctypes.CDLL] = None
+
+
+class TokenStrides(ctypes.Structure):
+    """ssd_token_strides_t: elements between consecutive tokens (0: contiguous)."""
+    _fields_ = [("x", ctypes.c_int64), ("dt", ctypes.c_int64), ("B", ctypes.c_int64),
+                ("C", ctypes.c_int64), ("y", ctypes.c_int64)]
 
 
 class SSDError(RuntimeError):
@@ -62,6 +69,9 @@ def library() -> ctypes.CDLL:
     lib.ssd_scan_varlen_fwd_states.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_states.argtypes = ([vp] * 12 + [i64, i32, i32, i32, i32, i32, i32, i32]
                                                + [vp, sz, vp])
+    lib.ssd_scan_varlen_fwd_strided.restype = ctypes.c_int
+    lib.ssd_scan_varlen_fwd_strided.argtypes = (lib.ssd_scan_varlen_fwd.argtypes[:21]
+                                                + [ctypes.POINTER(TokenStrides), vp, sz, vp])
     lib.ssd_scan_varlen_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_noalloc.argtypes = lib.ssd_scan_varlen_fwd.argtypes[:21] + [vp]
     lib.ssd_scan_varlen_read_errors.restype = ctypes.c_int
@@ -205,6 +215,52 @@ def ssd_scan_varlen_fwd_states(y, x, dt, A, B, C, D, dt_bias, initial_states,
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_scan_varlen_fwd_states")
+
+
+def _token_major(t, what: str, dtype, inner: int):
+    """Pointer and token stride of a token-major view whose rows (the trailing
+    `inner` elements) are contiguous."""
+    if t is None:
+        raise ValueError(f"{what} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{what} must have dtype {dtype}, got {t.dtype}")
+    if t.dim() < 2 or t[0].numel() != inner or (t.shape[0] > 0 and not t[0].is_contiguous()):
+        raise ValueError(f"{what}: each token's row must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()), t.stride(0)
+
+
+def ssd_scan_varlen_fwd_strided(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
+                                has_initial_state, cache_indices, *, chunk_size: int,
+                                dt_softplus: bool = True, workspace=None, stream=None) -> None:
+    """ssd_scan_varlen_fwd on token-major views with any token stride (e.g.
+    x, B, C, dt as column slices of a fused projection output, y a slice of a
+    wider buffer); each token's row must be contiguous."""
+    import torch
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    batch = query_start_loc.shape[0] - 1
+    if workspace is None:
+        raise ValueError("workspace is required (see ssd_scan_varlen_workspace_size)")
+    if has_initial_state is not None and has_initial_state.dtype == torch.bool:
+        has_initial_state = has_initial_state.view(torch.uint8)
+    py, sy = _token_major(y, "y", torch.bfloat16, H * P)
+    px, sx = _token_major(x, "x", torch.bfloat16, H * P)
+    pdt, sdt = _token_major(dt, "dt", torch.bfloat16, H)
+    pb, sb = _token_major(B, "B", torch.bfloat16, G * N)
+    pc, sc = _token_major(C, "C", torch.bfloat16, G * N)
+    strides = TokenStrides(sx, sdt, sb, sc, sy)
+    st = library().ssd_scan_varlen_fwd_strided(
+        py, px, pdt, _ptr(A, "A", torch.float32), pb, pc, _ptr(D, "D", torch.float32, True),
+        _ptr(dt_bias, "dt_bias", torch.float32, True), _ptr(ssm_pool, "ssm_pool", torch.float32),
+        _ptr(query_start_loc, "query_start_loc", torch.int32),
+        _ptr(has_initial_state, "has_initial_state", torch.uint8, True),
+        _ptr(cache_indices, "cache_indices"), T, batch, H, P, G, N, ssm_pool.shape[0],
+        int(chunk_size), int(bool(dt_softplus)), ctypes.byref(strides),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan_varlen_fwd_strided")
 
 
 def ssd_scan_varlen_fwd_noalloc(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,

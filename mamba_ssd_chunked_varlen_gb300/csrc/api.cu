@@ -124,7 +124,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                        int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim,
                        int32_t ngroups, int32_t dstate, int32_t chunk_size, int32_t dt_softplus,
                        void *workspace, size_t workspace_bytes, ssd_stream_t stream_,
-                       void *const *events)
+                       void *const *events, const TokenStrides *strides)
 {
     const ssd_status_t sz =
         check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size);
@@ -144,6 +144,18 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     if (total_len > 0 && (!aligned16(y) || !aligned16(x) || !aligned16(B) || !aligned16(C)))
         return SSD_ERR_INVALID_ARG;
     if (!aligned16(io.pool) || !aligned16(io.initial_states) || !aligned16(io.final_states))
+        return SSD_ERR_INVALID_ARG;
+    // token strides: at least the row of one token; TMA reads x, B, C with row
+    // pitches that are multiples of 16 bytes, and y rows are stored 16 bytes at a time
+    const int64_t HP = static_cast<int64_t>(nheads) * head_dim, GN = static_cast<int64_t>(ngroups) * dstate;
+    const TokenStrides ts{strides && strides->x ? strides->x : HP,
+                          strides && strides->dt ? strides->dt : nheads,
+                          strides && strides->B ? strides->B : GN,
+                          strides && strides->C ? strides->C : GN,
+                          strides && strides->y ? strides->y : HP};
+    if (ts.x < HP || ts.dt < nheads || ts.B < GN || ts.C < GN || ts.y < HP)
+        return SSD_ERR_INVALID_ARG;
+    if (ts.x % 8 || ts.B % 8 || ts.C % 8 || ts.y % 8)
         return SSD_ERR_INVALID_ARG;
     const int32_t Qb = ssd::block_tokens(chunk_size);
     const ssd::WsLayout L = ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, Qb);
@@ -171,6 +183,11 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.qsl = query_start_loc;
     p.has_init = has_initial_state;
     p.T = total_len;
+    p.x_ts = ts.x;
+    p.dt_ts = ts.dt;
+    p.B_ts = ts.B;
+    p.C_ts = ts.C;
+    p.y_ts = ts.y;
     p.batch = batch;
     p.H = nheads;
     p.P = head_dim;
@@ -192,11 +209,12 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     if (total_len > 0) {
         const uint64_t T = static_cast<uint64_t>(total_len);
         const uint64_t H = nheads, P = head_dim, G = ngroups, N = dstate;
-        bool ok = make_map_3d(&m1.B, B, N, G, T, N * 2, G * N * 2, 1, 64) &&
-                  make_map_3d(&m1.X, x, H * P, T, 1, H * P * 2, H * P * T * 2, 64, 1) &&
-                  make_map_3d(&m3.B, B, N, G, T, N * 2, G * N * 2, 1, 64) &&
-                  make_map_3d(&m3.C, C, N, G, T, N * 2, G * N * 2, 1, 64) &&
-                  make_map_3d(&m3.X, x, H * P, T, 1, H * P * 2, H * P * T * 2, 64, 1) &&
+        const uint64_t xs = ts.x * 2, bs = ts.B * 2, cs = ts.C * 2;   // token pitches, bytes
+        bool ok = make_map_3d(&m1.B, B, N, G, T, N * 2, bs, 1, 64) &&
+                  make_map_3d(&m1.X, x, H * P, T, 1, xs, xs * T, 64, 1) &&
+                  make_map_3d(&m3.B, B, N, G, T, N * 2, bs, 1, 64) &&
+                  make_map_3d(&m3.C, C, N, G, T, N * 2, cs, 1, 64) &&
+                  make_map_3d(&m3.X, x, H * P, T, 1, xs, xs * T, 64, 1) &&
                   make_map_3d(&m3.Sprev, p.sprev, N, P, static_cast<uint64_t>(L.max_chunks) * H,
                               N * 2, P * N * 2, 64, 1);
         if (!ok)
@@ -241,6 +259,29 @@ ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const f
     return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
                           total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
                           dt_softplus, workspace, workspace_bytes, stream, nullptr);
+}
+
+ssd_status_t ssd_scan_varlen_fwd_strided(void *y, const void *x, const void *dt, const float *A,
+                                         const void *B, const void *C, const float *D,
+                                         const float *dt_bias, float *ssm_pool,
+                                         const int32_t *query_start_loc,
+                                         const uint8_t *has_initial_state,
+                                         const uint32_t *cache_indices, int64_t total_len,
+                                         int32_t batch, int32_t nheads, int32_t head_dim,
+                                         int32_t ngroups, int32_t dstate, int64_t max_slots,
+                                         int32_t chunk_size, int32_t dt_softplus,
+                                         const ssd_token_strides_t *strides, void *workspace,
+                                         size_t workspace_bytes, ssd_stream_t stream)
+{
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    if (!ssm_pool && batch > 0)
+        return SSD_ERR_INVALID_ARG;
+    ssd::TokenStrides ts{0, 0, 0, 0, 0};
+    if (strides)
+        ts = ssd::TokenStrides{strides->x, strides->dt, strides->B, strides->C, strides->y};
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
+                          total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
+                          dt_softplus, workspace, workspace_bytes, stream, nullptr, &ts);
 }
 
 ssd_status_t ssd_scan_varlen_fwd_states(void *y, const void *x, const void *dt, const float *A,

@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int xoff = ((h0 + hh) * p.P - x_base) & 63;   // head's column in its X block
                 const uint32_t yd_col = kColYd + hh * P_pad + xoff;
                 const uint32_t yo_col = kColYo + (hh - gi * YG) * P_pad;
-                __nv_bfloat16 *yh = p.y + static_cast<int64_t>(t0) * p.H * p.P + (h0 + hh) * p.P;
+                __nv_bfloat16 *yh = p.y + static_cast<int64_t>(t0) * p.y_ts + (h0 + hh) * p.P;
                 for (int cb0 = 0; cb0 < p.P; cb0 += 64) {
                     const int col = cb0 + quarter * 16;   // this thread's 16 columns
                     if (col < p.P) {
@@ -540,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ch < nch && r < len) {
                             const uint4 v = *reinterpret_cast<const uint4 *>(sY + r * 128 +
                                                                              ((ch ^ (r & 7)) << 4));
-                            *reinterpret_cast<uint4 *>(yh + static_cast<int64_t>(r) * p.H * p.P +
-                                                       cb0 + ch * 8) = v;
+                            *reinterpret_cast<uint4 *>(yh + static_cast<int64_t>(r) * p.y_ts + cb0 +
+                                                       ch * 8) = v;
                         }
                     }
                     math_barrier();

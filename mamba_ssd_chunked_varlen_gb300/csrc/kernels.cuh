@@ -63,6 +63,12 @@ struct StateIO {
     float *final_states;          // (batch, H, P, N)
 };
 
+// Elements between consecutive tokens of x, dt, B, C and y (all rows of a
+// token stay contiguous); zero entries mean "contiguous".
+struct TokenStrides {
+    int64_t x, dt, B, C, y;
+};
+
 // The whole scan (argument checks, tensor maps, the three launches) on a
 // caller-provided scratch buffer; `events` (4 CUDA events) may be null.
 ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
@@ -71,7 +77,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                        int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim,
                        int32_t ngroups, int32_t dstate, int32_t chunk_size, int32_t dt_softplus,
                        void *workspace, size_t workspace_bytes, ssd_stream_t stream,
-                       void *const *events);
+                       void *const *events, const TokenStrides *strides = nullptr);
 
 inline int pad64(int v) { return (v + 63) / 64 * 64; }
 

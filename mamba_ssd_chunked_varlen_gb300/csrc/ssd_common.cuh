@@ -87,6 +87,9 @@ struct ScanParams {
     const int32_t *qsl;
     const uint8_t *has_init;  // may be null
     int64_t T;
+    // elements between consecutive tokens (H*P, H, G*N, G*N, H*P when contiguous;
+    // larger for column slices of a wider buffer, e.g. a fused projection output)
+    int64_t x_ts, dt_ts, B_ts, C_ts, y_ts;
     int32_t batch, H, P, G, N;
     int32_t Q;            // tokens per block (block_tokens of the chunk size)
     int64_t max_slots;

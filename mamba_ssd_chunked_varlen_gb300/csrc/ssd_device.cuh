@@ -39,7 +39,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 // Processed step of token t, head h: softplus(dt + dt_bias) (or dt + dt_bias).
 __device__ __forceinline__ float processed_dt(const ScanParams &p, int64_t t, int h)
 {
-    float v = __bfloat162float(p.dt[t * p.H + h]);
+    float v = __bfloat162float(p.dt[t * p.dt_ts + h]);
     if (p.dt_bias)
         v += p.dt_bias[h];
     return p.dt_softplus ? softplus_f32(v) : v;
