@@ -276,6 +276,9 @@ def run_ours(args, rank, world, local):
         # rows of its sequences, final_states a (batch, H, P, N) output
         init_states = d["pool"][d["cidx"].long()].contiguous()
         final_states = torch.empty_like(init_states)
+    if args.form == "bf16pool":
+        # the pool stored in bf16 (same values rounded once)
+        pool_bf16 = d["pool"].to(torch.bfloat16)
     if args.form == "strided":
         # x, B, C, dt as column slices of one fused projection output
         # [x | B | C | dt | pad] per token (y stays contiguous)
@@ -300,6 +303,12 @@ def run_ours(args, rank, world, local):
                 yy if yy is not None else y, sv["x"], sv["dt"], d["A"], sv["B"], sv["C"], d["D"],
                 d["dt_bias"], d["pool"], d["qsl"], d["hinit"], d["cidx"], chunk_size=w.chunk_size,
                 dt_softplus=w.dt_softplus, workspace=ws, stream=stream)
+            return
+        if args.form == "bf16pool":
+            pkg.ssd_scan_varlen_fwd_bf16_pool(
+                yy if yy is not None else y, dd["x"], dd["dt"], d["A"], dd["B"], dd["C"], d["D"],
+                d["dt_bias"], pool_bf16, dd["qsl"], dd["hinit"], dd["cidx"],
+                chunk_size=w.chunk_size, dt_softplus=w.dt_softplus, workspace=ws, stream=stream)
             return
         if args.form == "states":
             pkg.ssd_scan_varlen_fwd_states(
@@ -513,11 +522,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="kernelindex", choices=W.WORKLOADS)
-    ap.add_argument("--form", choices=("inplace", "states", "strided"), default="inplace",
+    ap.add_argument("--form", choices=("inplace", "states", "strided", "bf16pool"),
+                    default="inplace",
                     help="inplace: ssd_scan_varlen_fwd (slot pool); states: "
                          "ssd_scan_varlen_fwd_states (separate initial/final state arrays); "
                          "strided: ssd_scan_varlen_fwd_strided on x, B, C, dt cut from one "
                          "fused projection buffer (the e2e leg copies contiguous inputs); "
+                         "bf16pool: ssd_scan_varlen_fwd_bf16_pool (bf16 slot pool); "
                          "the per-stage attribution always uses the in-place profiled call")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")

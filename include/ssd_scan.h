@@ -118,6 +118,20 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd(
     int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
     void *workspace, size_t workspace_bytes, ssd_stream_t stream);
 
+/* ssd_scan_varlen_fwd with a bf16 slot pool: ssm_pool is bf16 (max_slots,
+ * nheads, head_dim, dstate), the storage type the "Mamba2SSDChunkScanVarlenFwd
+ * Inplace" tensor shapes allow besides fp32 ("storage dtype only; the scan
+ * accumulates in fp32").  Initial states are widened to fp32 when read; final
+ * states are rounded to bf16 (nearest even) when written.  Other arguments,
+ * results and errors as ssd_scan_varlen_fwd. */
+SSD_API ssd_status_t ssd_scan_varlen_fwd_bf16_pool(
+    void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, const float *dt_bias, void *ssm_pool, const int32_t *query_start_loc,
+    const uint8_t *has_initial_state, const uint32_t *cache_indices,
+    int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim, int32_t ngroups,
+    int32_t dstate, int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
+    void *workspace, size_t workspace_bytes, ssd_stream_t stream);
+
 /* Elements (not bytes) between consecutive tokens of each token-major input
  * and of y; 0 means contiguous (H*P for x and y, H for dt, G*N for B and C).
  * Within a token, x / y rows stay (H, P) contiguous, B / C rows (G, N) and dt

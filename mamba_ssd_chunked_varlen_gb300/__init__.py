@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     ssd_scan_varlen_fwd_profiled,
     ssd_scan_varlen_fwd_states,
     ssd_scan_varlen_fwd_strided,
+    ssd_scan_varlen_fwd_bf16_pool,
     ssd_scan_varlen_fwd_noalloc,
     ssd_scan_varlen_num_launches,
     ssd_scan_varlen_read_errors,

@@ -21,6 +21,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_fwd_profiled",
     "ssd_scan_varlen_fwd_states",
     "ssd_scan_varlen_fwd_strided",
+    "ssd_scan_varlen_fwd_bf16_pool",
     "ssd_scan_varlen_fwd_noalloc",
     "ssd_scan_varlen_read_errors",
     "ssd_status_string",
@@ -72,6 +73,8 @@ def library() -> ctypes.CDLL:
     lib.ssd_scan_varlen_fwd_strided.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_strided.argtypes = (lib.ssd_scan_varlen_fwd.argtypes[:21]
                                                 + [ctypes.POINTER(TokenStrides), vp, sz, vp])
+    lib.ssd_scan_varlen_fwd_bf16_pool.restype = ctypes.c_int
+    lib.ssd_scan_varlen_fwd_bf16_pool.argtypes = lib.ssd_scan_varlen_fwd.argtypes
     lib.ssd_scan_varlen_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_noalloc.argtypes = lib.ssd_scan_varlen_fwd.argtypes[:21] + [vp]
     lib.ssd_scan_varlen_read_errors.restype = ctypes.c_int
@@ -119,8 +122,9 @@ def _stream_handle(stream) -> ctypes.c_void_p:
 
 
 def _fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
-              cache_indices, chunk_size, dt_softplus, workspace, stream):
+              cache_indices, chunk_size, dt_softplus, workspace, stream, pool_dtype=None):
     import torch
+    pool_dtype = torch.float32 if pool_dtype is None else pool_dtype
     T, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
     batch = query_start_loc.shape[0] - 1
@@ -135,8 +139,8 @@ def _fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_init
         _ptr(dt, "dt", torch.bfloat16), _ptr(A, "A", torch.float32),
         _ptr(B, "B", torch.bfloat16), _ptr(C, "C", torch.bfloat16),
         _ptr(D, "D", torch.float32, True), _ptr(dt_bias, "dt_bias", torch.float32, True),
-        _ptr(ssm_pool, "ssm_pool", torch.float32), _ptr(query_start_loc, "query_start_loc",
-                                                        torch.int32),
+        _ptr(ssm_pool, "ssm_pool", pool_dtype), _ptr(query_start_loc, "query_start_loc",
+                                                     torch.int32),
         _ptr(has_initial_state, "has_initial_state", torch.uint8, True),
         _ptr(cache_indices, "cache_indices"),
         T, batch, H, P, G, N, ssm_pool.shape[0], int(chunk_size), int(bool(dt_softplus)),
@@ -261,6 +265,20 @@ def ssd_scan_varlen_fwd_strided(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_s
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_scan_varlen_fwd_strided")
+
+
+def ssd_scan_varlen_fwd_bf16_pool(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,
+                                  has_initial_state, cache_indices, *, chunk_size: int,
+                                  dt_softplus: bool = True, workspace=None, stream=None) -> None:
+    """ssd_scan_varlen_fwd with a bf16 ssm_pool (slots, H, P, N): initial states
+    widened to fp32 on read, final states rounded to bf16 on write."""
+    import torch
+    st = library().ssd_scan_varlen_fwd_bf16_pool(
+        *_fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
+                   cache_indices, chunk_size, dt_softplus, workspace, stream,
+                   pool_dtype=torch.bfloat16))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan_varlen_fwd_bf16_pool")
 
 
 def ssd_scan_varlen_fwd_noalloc(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc,

@@ -176,6 +176,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.D = D;
     p.dt_bias = dt_bias;
     p.pool = io.pool;
+    p.pool_bf16 = io.pool_bf16;
     p.cache_idx = io.cache_indices;
     p.max_slots = io.max_slots;
     p.init_states = io.initial_states;
@@ -253,7 +254,27 @@ ssd_status_t ssd_scan_varlen_fwd(void *y, const void *x, const void *dt, const f
                                  int64_t max_slots, int32_t chunk_size, int32_t dt_softplus,
                                  void *workspace, size_t workspace_bytes, ssd_stream_t stream)
 {
-    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr, 0};
+    if (!ssm_pool && batch > 0)
+        return SSD_ERR_INVALID_ARG;
+    return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
+                          total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
+                          dt_softplus, workspace, workspace_bytes, stream, nullptr);
+}
+
+ssd_status_t ssd_scan_varlen_fwd_bf16_pool(void *y, const void *x, const void *dt, const float *A,
+                                           const void *B, const void *C, const float *D,
+                                           const float *dt_bias, void *ssm_pool,
+                                           const int32_t *query_start_loc,
+                                           const uint8_t *has_initial_state,
+                                           const uint32_t *cache_indices, int64_t total_len,
+                                           int32_t batch, int32_t nheads, int32_t head_dim,
+                                           int32_t ngroups, int32_t dstate, int64_t max_slots,
+                                           int32_t chunk_size, int32_t dt_softplus,
+                                           void *workspace, size_t workspace_bytes,
+                                           ssd_stream_t stream)
+{
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr, 1};
     if (!ssm_pool && batch > 0)
         return SSD_ERR_INVALID_ARG;
     return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
@@ -273,7 +294,7 @@ ssd_status_t ssd_scan_varlen_fwd_strided(void *y, const void *x, const void *dt,
                                          const ssd_token_strides_t *strides, void *workspace,
                                          size_t workspace_bytes, ssd_stream_t stream)
 {
-    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr, 0};
     if (!ssm_pool && batch > 0)
         return SSD_ERR_INVALID_ARG;
     ssd::TokenStrides ts{0, 0, 0, 0, 0};
@@ -294,7 +315,7 @@ ssd_status_t ssd_scan_varlen_fwd_states(void *y, const void *x, const void *dt, 
                                         int32_t dt_softplus, void *workspace,
                                         size_t workspace_bytes, ssd_stream_t stream)
 {
-    const ssd::StateIO io{nullptr, nullptr, 0, initial_states, final_states};
+    const ssd::StateIO io{nullptr, nullptr, 0, initial_states, final_states, 0};
     return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,
                           total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
                           dt_softplus, workspace, workspace_bytes, stream, nullptr);
@@ -313,7 +334,7 @@ ssd_status_t ssd_scan_varlen_fwd_profiled(
     for (int k = 0; k < 4; ++k)
         if (!events[k])
             return SSD_ERR_INVALID_ARG;
-    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr, 0};
     if (!ssm_pool && batch > 0)
         return SSD_ERR_INVALID_ARG;
     return ssd::scan_impl(y, x, dt, A, B, C, D, dt_bias, io, query_start_loc, has_initial_state,

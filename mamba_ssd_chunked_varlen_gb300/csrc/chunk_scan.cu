@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = h0 / (p.H / p.G);
     const int nkb = N_pad / 64;
     // the state entering the block is zero for a first block without initial state
-    const bool has_prev = !bi.first || seq_init_state(p, bi.seq) != nullptr;
+    const bool has_prev = !bi.first || seq_init_index(p, bi.seq) >= 0;
     // X columns of the CTA's heads, loaded from a 64-aligned start
     const int x_base = (h0 * p.P / 64) * 64;
     const int n_xb = ((h0 + HB) * p.P - x_base + 63) / 64;

@@ -56,11 +56,12 @@ cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps, cu
 // "Mamba2SSDChunkScanVarlenFwdInplace") when pool is set, else separate
 // per-sequence arrays (the final_states form of "mamba2_ssd_scan").
 struct StateIO {
-    float *pool;                  // (max_slots, H, P, N) or null
+    void *pool;                   // (max_slots, H, P, N) fp32 (bf16 when pool_bf16) or null
     const uint32_t *cache_indices;
     int64_t max_slots;
     const float *initial_states;  // (batch, H, P, N) or null (zero initial states)
     float *final_states;          // (batch, H, P, N)
+    int pool_bf16;                // 1: the pool stores bf16
 };
 
 // Elements between consecutive tokens of x, dt, B, C and y (all rows of a

@@ -55,7 +55,7 @@ extern "C" ssd_status_t ssd_scan_varlen_fwd_noalloc(
 {
     const size_t need = ssd_scan_varlen_workspace_size(total_len, batch, nheads, head_dim,
                                                        ngroups, dstate, chunk_size);
-    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr};
+    const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr, 0};
     if (!ssm_pool && batch > 0)
         return SSD_ERR_INVALID_ARG;
     if (need == 0)  // invalid or unsupported sizes: let the full check name the reason

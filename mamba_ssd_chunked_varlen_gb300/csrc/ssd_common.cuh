@@ -80,7 +80,8 @@ struct ScanParams {
     // where each sequence's state starts and ends: either the slot pool
     // (in place: pool, cache_idx, max_slots) or, when pool is null, separate
     // per-sequence arrays (init_states may be null: zero initial states)
-    float *pool;
+    void *pool;                // fp32, or bf16 when pool_bf16
+    int32_t pool_bf16;         // 1: the pool stores bf16 (the scan accumulates in fp32)
     const uint32_t *cache_idx;
     const float *init_states;  // (batch, H, P, N) or null
     float *final_states;       // (batch, H, P, N)

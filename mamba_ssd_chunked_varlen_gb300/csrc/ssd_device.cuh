@@ -60,35 +60,65 @@ __device__ __forceinline__ T warp_inclusive_scan(T v)
 }
 
 // ---------------------------------------------------------------- state I/O
-// Sequence b's initial state (null: zero).  In place ("Mamba2SSDChunkScanVarlen
-// FwdInplace"): its pool slot when has_initial_state[b] is set and the slot
-// index is in range.  Separate arrays (the "mamba2_ssd_scan" final_states
-// form): initial_states[b] unless has_initial_state is given and false.
-__device__ __forceinline__ const float *seq_init_state(const ScanParams &p, int b)
+// Element index of sequence b's initial state row (-1: zero initial state).
+// In place ("Mamba2SSDChunkScanVarlenFwdInplace"): its pool slot when
+// has_initial_state[b] is set and the slot index is in range.  Separate arrays
+// (the "mamba2_ssd_scan" final_states form): row b of initial_states unless
+// has_initial_state is given and false.
+__device__ __forceinline__ int64_t seq_init_index(const ScanParams &p, int b)
 {
     const int64_t slot_elems = static_cast<int64_t>(p.H) * p.P * p.N;
     const bool flag = p.has_init == nullptr || p.has_init[b] != 0;
     if (p.pool != nullptr) {
         const uint32_t slot = p.cache_idx[b];
         return (p.has_init != nullptr && flag && static_cast<int64_t>(slot) < p.max_slots)
-                   ? p.pool + static_cast<int64_t>(slot) * slot_elems
-                   : nullptr;
+                   ? static_cast<int64_t>(slot) * slot_elems
+                   : -1;
     }
-    return (p.init_states != nullptr && flag) ? p.init_states + static_cast<int64_t>(b) * slot_elems
-                                              : nullptr;
+    return (p.init_states != nullptr && flag) ? static_cast<int64_t>(b) * slot_elems : -1;
 }
 
-// Where sequence b's final state goes (null: nowhere, an out-of-range slot).
-__device__ __forceinline__ float *seq_final_state(const ScanParams &p, int b)
+// Element index of the row that receives sequence b's final state (-1: none,
+// an out-of-range slot).
+__device__ __forceinline__ int64_t seq_final_index(const ScanParams &p, int b)
 {
     const int64_t slot_elems = static_cast<int64_t>(p.H) * p.P * p.N;
     if (p.pool != nullptr) {
         const uint32_t slot = p.cache_idx[b];
-        return static_cast<int64_t>(slot) < p.max_slots
-                   ? p.pool + static_cast<int64_t>(slot) * slot_elems
-                   : nullptr;
+        return static_cast<int64_t>(slot) < p.max_slots ? static_cast<int64_t>(slot) * slot_elems
+                                                         : -1;
     }
-    return p.final_states + static_cast<int64_t>(b) * slot_elems;
+    return static_cast<int64_t>(b) * slot_elems;
+}
+
+// Four consecutive state elements from the initial-state storage (the pool,
+// fp32 or bf16, or initial_states), widened to fp32.
+__device__ __forceinline__ float4 load_init4(const ScanParams &p, int64_t i)
+{
+    if (p.pool == nullptr)
+        return *reinterpret_cast<const float4 *>(p.init_states + i);
+    if (!p.pool_bf16)
+        return *reinterpret_cast<const float4 *>(static_cast<const float *>(p.pool) + i);
+    const uint2 raw = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p.pool) + i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+    const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+    return make_float4(a.x, a.y, c.x, c.y);
+}
+
+// Four consecutive final-state elements into their storage (bf16 storage
+// rounds to nearest even).
+__device__ __forceinline__ void store_final4(const ScanParams &p, int64_t i, float4 v)
+{
+    if (p.pool == nullptr) {
+        *reinterpret_cast<float4 *>(p.final_states + i) = v;
+    } else if (!p.pool_bf16) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(p.pool) + i) = v;
+    } else {
+        uint2 packed;
+        packed.x = pack_bf16(v.x, v.y);
+        packed.y = pack_bf16(v.z, v.w);
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.pool) + i) = packed;
+    }
 }
 
 // ---------------------------------------------------------------- block map

@@ -45,13 +45,12 @@ __global__ void __launch_bounds__(kThreads, 4) state_passing_kernel(ScanParams p
     if (b >= p.batch || e >= PN)
         return;
 
-    const float *init = seq_init_state(p, b);
-    float *fin = seq_final_state(p, b);
+    const int64_t init = seq_init_index(p, b), fin = seq_final_index(p, b);
     const int64_t off = static_cast<int64_t>(h) * PN + e;
 
     float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (init)
-        S = *reinterpret_cast<const float4 *>(init + off);
+    if (init >= 0)
+        S = load_init4(p, init + off);
 
     const int c_begin = p.seq_first[b], c_end = p.seq_first[b + 1];
     const int64_t stride = static_cast<int64_t>(p.H) * PN;
@@ -85,8 +84,8 @@ __global__ void __launch_bounds__(kThreads, 4) state_passing_kernel(ScanParams p
         sp += kAhead * stride;
         dec += static_cast<int64_t>(kAhead) * p.H;
     }
-    if (fin)
-        *reinterpret_cast<float4 *>(fin + off) = S;
+    if (fin >= 0)
+        store_final4(p, fin + off, S);
     if (threadIdx.x == 0)
         SSD_TRACE_EV(1, 2);
 }
