@@ -54,6 +54,20 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Whether a call may hold sequences of at most kShortLenMax tokens (then the
+// short-sequence kernel runs): a batch of several sequences, or one sequence
+// that short.  A single longer sequence needs no such launch.
+bool short_path(int64_t total_len, int32_t batch)
+{
+    return batch > 1 || total_len <= ssd::kShortLenMax;
+}
+
+// Sequences of at most this many tokens go to the short-sequence kernel.
+int32_t short_len_of(int64_t total_len, int32_t batch)
+{
+    return short_path(total_len, batch) ? ssd::kShortLenMax : 0;
+}
+
 ssd_status_t check_sizes(int64_t T, int32_t batch, int32_t H, int32_t P, int32_t G, int32_t N,
                          int32_t Q)
 {
@@ -104,14 +118,14 @@ size_t ssd_scan_varlen_workspace_size(int64_t total_len, int32_t batch, int32_t 
     if (check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size) != SSD_OK)
         return 0;
     return ssd::ws_layout(total_len, batch, nheads, head_dim, dstate,
-                          ssd::block_tokens(chunk_size)).total;
+                          ssd::block_tokens(chunk_size), short_len_of(total_len, batch)).total;
 }
 
 int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
 {
     if (batch <= 0)
         return 0;
-    return total_len > 0 ? 3 : 2;
+    return 2 + (total_len > 0 ? 1 : 0) + (short_path(total_len, batch) ? 1 : 0);
 }
 
 }  // extern "C"
@@ -158,7 +172,8 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     if (ts.x % 8 || ts.B % 8 || ts.C % 8 || ts.y % 8)
         return SSD_ERR_INVALID_ARG;
     const int32_t Qb = ssd::block_tokens(chunk_size);
-    const ssd::WsLayout L = ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, Qb);
+    const ssd::WsLayout L =
+        ssd::ws_layout(total_len, batch, nheads, head_dim, dstate, Qb, short_len_of(total_len, batch));
     if (!workspace || workspace_bytes < L.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return SSD_ERR_WORKSPACE;
@@ -172,6 +187,8 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.y = static_cast<__nv_bfloat16 *>(y);
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.dt = static_cast<const __nv_bfloat16 *>(dt);
+    p.B = static_cast<const __nv_bfloat16 *>(B);
+    p.C = static_cast<const __nv_bfloat16 *>(C);
     p.A = A;
     p.D = D;
     p.dt_bias = dt_bias;
@@ -196,9 +213,12 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.N = dstate;
     p.Q = Qb;
     p.dt_softplus = dt_softplus ? 1 : 0;
+    p.short_len = short_len_of(total_len, batch);
     p.max_chunks = static_cast<int32_t>(L.max_chunks);
     p.hdr = reinterpret_cast<ssd::WsHeader *>(ws + L.header);
     p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);
+    p.short_list = reinterpret_cast<ssd::SeqRec *>(ws + L.short_list);
+    p.long_list = reinterpret_cast<ssd::SeqRec *>(ws + L.long_list);
     p.decay = reinterpret_cast<float *>(ws + L.decay);
     p.schunk = reinterpret_cast<float *>(ws + L.schunk);
     p.sprev = reinterpret_cast<__nv_bfloat16 *>(ws + L.sprev);
@@ -234,6 +254,8 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     if (ssd::launch_state_passing(p, stream, pdl) != cudaSuccess || !mark(2))
         return SSD_ERR_CUDA;
     if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream, pdl) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (p.short_len > 0 && ssd::launch_short_scan(p, stream, pdl) != cudaSuccess)
         return SSD_ERR_CUDA;
     if (!mark(3))
         return SSD_ERR_CUDA;

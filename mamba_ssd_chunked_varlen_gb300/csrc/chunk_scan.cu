@@ -175,8 +175,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmS);
     }
     const BlockInfo bi = map_block<kThreads>(p, blk, scratch, nullptr);
-    if (!bi.valid || bi.seq < 0)
+    // Every CTA waits for the state-passing grid before it leaves (those without
+    // an entering state would not otherwise), so that this grid completes only
+    // after its predecessors and a dependent launch may rely on all of them.
+    if (!bi.valid || bi.seq < 0) {
+        pdl_wait();
         return;
+    }
     const int t0 = bi.t0, len = bi.len;
     const int g = h0 / (p.H / p.G);
     const int nkb = N_pad / 64;
@@ -561,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *s_abort = 1;
     }
 
+    pdl_wait();
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (tid == 0)

@@ -91,9 +91,9 @@ __global__ void __launch_bounds__(kThreads)
     const int h0 = blockIdx.y * HB;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // The per-call bookkeeping (block table, error word, slot checks) falls to
-    // CTA (max_chunks - 1, 0): the number of blocks is sum_b ceil(L_b / Q) <
-    // T / Q + batch <= max_chunks, so that CTA never holds a block and the
-    // bookkeeping delays no block's work.
+    // CTA (max_chunks - 1, 0): max_chunks bounds the number of blocks from
+    // above with its last index always free, so that CTA never holds a block
+    // and the bookkeeping delays no block's work.
     const bool leader = blockIdx.x == gridDim.x - 1 && blockIdx.y == 0;
     if (tid == 0)
         SSD_TRACE_EV(0, 0);
@@ -111,6 +111,35 @@ __global__ void __launch_bounds__(kThreads)
             for (int b = tid; b < p.batch; b += kThreads)
                 if (static_cast<int64_t>(p.cache_idx[b]) >= p.max_slots)
                     record_error(p.hdr, kErrBadSlot);
+        // the work lists: short sequences for the short-sequence kernel, the
+        // others for state passing
+        {
+            int32_t *s_count = scratch + 38, *l_count = scratch + 39;   // past map_block's ints
+            if (tid == 0) {
+                *s_count = 0;
+                *l_count = 0;
+            }
+            __syncthreads();   // also orders map_block's seq_first writes before the reads
+            if (bi.valid)
+                for (int b = tid; b < p.batch; b += kThreads) {
+                    SeqRec r;
+                    r.t0 = p.qsl[b];
+                    r.len = p.qsl[b + 1] - r.t0;
+                    r.c_begin = p.seq_first[b];
+                    r.c_end = p.seq_first[b + 1];
+                    r.init = seq_init_index(p, b);
+                    r.fin = seq_final_index(p, b);
+                    if (r.len <= p.short_len)
+                        p.short_list[atomicAdd(s_count, 1)] = r;
+                    else
+                        p.long_list[atomicAdd(l_count, 1)] = r;
+                }
+            __syncthreads();
+            if (tid == 0) {
+                p.hdr->n_short = *s_count;
+                p.hdr->n_long = *l_count;
+            }
+        }
         if (tid == 0) {
             if (!bi.valid)
                 record_error(p.hdr, kErrBadQsl);

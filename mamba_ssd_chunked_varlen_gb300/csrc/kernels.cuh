@@ -33,6 +33,15 @@ cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
 // launched as a programmatic dependent of the previous kernel.
 cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool programmatic);
 
+// Short sequences (<= p.short_len <= kShortLenMax tokens, including empty
+// ones): the per-token recurrence with the state in registers, y and the final
+// state written directly.  Launched after the chunk-state kernel's checks.
+// Its cost grows with the tokens while the chunked kernels spend a whole
+// 128-row block on any sequence; measured on GB300 (batches of 256 sequences,
+// 64 heads of 64 x 128) the per-token path wins up to about 8 tokens.
+constexpr int kShortLenMax = 8;
+cudaError_t launch_short_scan(const ScanParams &p, cudaStream_t stream, bool programmatic);
+
 // Stages 2a/2b/4: per (block, head group) C.B^T, the masked diagonal block,
 // the off-diagonal C.S_prev^T term and the D skip; writes y.
 struct ChunkScanMaps {

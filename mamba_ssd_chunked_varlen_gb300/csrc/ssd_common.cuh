@@ -22,15 +22,26 @@ struct WsHeader {
     uint32_t errors;   // SSD_DEVERR_* bits of the current call
     int32_t nchunks;   // blocks of the call
     int32_t valid;     // 1 when query_start_loc passed the device checks
-    int32_t pad[61];
+    int32_t n_short;   // entries of the short-sequence work list
+    int32_t n_long;    // entries of the state-passing work list
+    int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
 // Byte offsets of the workspace regions; every region is 256-byte aligned.
 struct WsLayout {
     int64_t max_chunks;
-    size_t header, seq_first, decay, schunk, sprev, total;
+    size_t header, seq_first, short_list, long_list, decay, schunk, sprev, total;
 };
+
+// One sequence of a work list, resolved by the chunk-state kernel's
+// bookkeeping CTA so that a consumer reaches all of it with one 32-byte read.
+struct __align__(16) SeqRec {
+    int32_t t0, len;          // its tokens
+    int32_t c_begin, c_end;   // its blocks
+    int64_t init, fin;        // element index of its initial / final state (-1: none)
+};
+static_assert(sizeof(SeqRec) == 32, "record size");
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -41,24 +52,36 @@ __host__ __device__ inline int32_t block_tokens(int32_t chunk_size)
     return chunk_size < 128 ? chunk_size : 128;
 }
 
-// Upper bound on the number of blocks: sum_b ceil(L_b / Q) <= ceil(T / Q) + batch.
-__host__ __device__ inline int64_t max_chunks_bound(int64_t T, int32_t batch, int32_t Q)
+// Upper bound on the number of blocks.  Only sequences longer than short_len
+// tokens are cut into blocks (the short-sequence kernel takes the others), and
+// at most n = min(batch, T / (short_len + 1)) sequences are that long, so
+//   sum_b ceil(L_b / Q) < T / Q + n <= ceil(T / Q) + n:
+// the bound's last block index never holds a block.  At least 1.
+__host__ __device__ inline int64_t max_chunks_bound(int64_t T, int32_t batch, int32_t Q,
+                                                    int32_t short_len)
 {
-    return (T + Q - 1) / Q + batch;
+    const int64_t by_len = T / (static_cast<int64_t>(short_len) + 1);
+    const int64_t n_long = by_len < batch ? by_len : batch;
+    const int64_t bound = (T + Q - 1) / Q + n_long;
+    return bound > 0 ? bound : 1;
 }
 
 // Q here is the block size (block_tokens of the chunk size).
 __host__ __device__ inline WsLayout ws_layout(int64_t T, int32_t batch, int32_t H, int32_t P,
-                                              int32_t N, int32_t Q)
+                                              int32_t N, int32_t Q, int32_t short_len)
 {
     WsLayout L;
-    L.max_chunks = max_chunks_bound(T, batch, Q);
+    L.max_chunks = max_chunks_bound(T, batch, Q, short_len);
     const size_t mc = static_cast<size_t>(L.max_chunks);
     size_t off = 0;
     L.header = off;
     off = align256(off + sizeof(WsHeader));
     L.seq_first = off;
     off = align256(off + sizeof(int32_t) * (static_cast<size_t>(batch) + 1));
+    L.short_list = off;
+    off = align256(off + sizeof(SeqRec) * static_cast<size_t>(batch));
+    L.long_list = off;
+    off = align256(off + sizeof(SeqRec) * static_cast<size_t>(batch));
     L.decay = off;
     off = align256(off + sizeof(float) * mc * H);
     L.schunk = off;
@@ -74,6 +97,7 @@ struct ScanParams {
     __nv_bfloat16 *y;
     const __nv_bfloat16 *x;
     const __nv_bfloat16 *dt;
+    const __nv_bfloat16 *B, *C;   // read directly only by the short-sequence kernel
     const float *A;
     const float *D;        // may be null
     const float *dt_bias;  // may be null
@@ -95,10 +119,14 @@ struct ScanParams {
     int32_t Q;            // tokens per block (block_tokens of the chunk size)
     int64_t max_slots;
     int32_t dt_softplus;
+    int32_t short_len;    // sequences of at most this many tokens go to the short-sequence
+                          // kernel (the chunked kernels skip them); 0: none
     int32_t max_chunks;   // upper bound on the number of blocks
     // workspace regions
     WsHeader *hdr;
     int32_t *seq_first;   // (batch + 1): first block of each sequence, then the total
+    SeqRec *short_list;   // the short sequences (hdr->n_short of them)
+    SeqRec *long_list;    // the other sequences (hdr->n_long), state passing's list
     float *decay;         // [block][head] exp(sum of A*dt over the block)
     float *schunk;        // [block][head][P][N] block states (zero initial state)
     __nv_bfloat16 *sprev; // [block][head][P][N] state entering each block (bf16 operand)

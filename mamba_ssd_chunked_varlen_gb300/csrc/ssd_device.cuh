@@ -129,13 +129,14 @@ struct BlockInfo {
     int32_t t0;      // first token
     int32_t len;     // tokens in the block (1..blk_len)
     int32_t first;   // 1 when this is the sequence's first block
+    int32_t last;    // 1 when this is the sequence's last block
     int32_t valid;   // 0 when query_start_loc failed the checks
     int32_t total;   // number of blocks of the whole call
 };
 
 // Maps block `blk` by scanning query_start_loc.  Called by every thread of a
 // CTA of kThreads threads (kThreads a multiple of 32, <= 1024); uses `scratch`
-// (>= 40 ints of shared memory).  When `seq_first` is non-null the CTA also
+// (ints 0-36 of shared memory).  When `seq_first` is non-null the CTA also
 // writes every sequence's first block index there (and the total at [batch]).
 // One pass over query_start_loc per kThreads sequences: the checks of its
 // first and last entries ride along with the loads of the scan.
@@ -146,7 +147,7 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
     constexpr int kWarps = kThreads / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int32_t *s_warp = scratch;        // kWarps partial sums
-    int32_t *s_res = scratch + 32;    // 4 result ints, written by the owning thread
+    int32_t *s_res = scratch + 32;    // 5 result ints, written by the owning thread
     int32_t carry = 0;
     int bad = 0;
     for (int base = 0; base < p.batch; base += kThreads) {
@@ -161,7 +162,8 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
                 bad = 1;
                 len = 0;
             }
-            n = (len + p.Q - 1) / p.Q;
+            // a sequence short enough for the short-sequence kernel holds no block
+            n = len <= p.short_len ? 0 : (len + p.Q - 1) / p.Q;
         }
         const int32_t incl = warp_inclusive_scan(n);
         if (lane == 31)
@@ -184,6 +186,7 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
                 s_res[1] = start + k * p.Q;
                 s_res[2] = min(p.Q, len - k * p.Q);
                 s_res[3] = k == 0;
+                s_res[4] = k == n - 1;
             }
         }
         carry += total;
@@ -200,6 +203,7 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
     bi.t0 = mine ? s_res[1] : 0;
     bi.len = mine ? s_res[2] : 0;
     bi.first = mine ? s_res[3] : 0;
+    bi.last = mine ? s_res[4] : 0;
     return bi;
 }
 

@@ -162,7 +162,7 @@ def _ragged_lengths(rng: np.random.Generator, n: int, lo: int, hi: int, avoid_mu
 
 
 # Workload names, in the order they are listed for this op.
-WORKLOADS = ("tiny", "kernelindex", "ragged", "nemotron_h", "serving_mix")
+WORKLOADS = ("tiny", "kernelindex", "ragged", "nemotron_h", "serving_mix", "decode")
 
 
 def workload(name: str, seed: Optional[int] = None) -> Workload:
@@ -179,6 +179,9 @@ def workload(name: str, seed: Optional[int] = None) -> Workload:
                   pool, every sequence with an initial state.
     serving_mix   256 sequences, geometric lengths with mean 64, H=64, P=64, G=1,
                   N=128, chunk 256, 512-slot pool, initial state with p = 0.8.
+    decode        256 sequences of 1 token each (a decode step of the serving
+                  shape: H=64, P=64, G=1, N=128, chunk 256, 512-slot pool), every
+                  sequence with an initial state: the pool read-modify-write case.
 
     For tiny and kernelindex the pool has 4 slots and one random slot is
     written, so that the untouched-slot check has something to check.
@@ -200,6 +203,9 @@ def workload(name: str, seed: Optional[int] = None) -> Workload:
         lens = np.random.default_rng([seed, 1]).geometric(1.0 / 64.0, 256)
         return make_workload(name, lens, 64, 64, 1, 128, 256, max_slots=512, seed=seed,
                              has_init_p=0.8)
+    if name == "decode":
+        return make_workload(name, [1] * 256, 64, 64, 1, 128, 256, max_slots=512, seed=seed,
+                             has_init_p=1.0)
     raise KeyError(name)
 
 
