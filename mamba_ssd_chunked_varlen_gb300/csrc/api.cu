@@ -35,6 +35,24 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// 3-D bf16 tensor map with a {b0, b1, b2} box and no swizzle (rows land
+// packed in shared memory).  Elements outside the tensor read as zero.
+bool make_map_plain(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+                    uint32_t b2)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 tensor map with a {64, b1, b2} box and 128-byte swizzle.  Elements
 // outside the tensor read as zero.
 bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
@@ -225,8 +243,10 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
 
     ssd::ChunkStateMaps m1;
     ssd::ChunkScanMaps m3;
+    ssd::ShortScanMaps ms;
     std::memset(&m1, 0, sizeof m1);  // with total_len == 0 no kernel reads a map
     std::memset(&m3, 0, sizeof m3);
+    std::memset(&ms, 0, sizeof ms);
     if (total_len > 0) {
         const uint64_t T = static_cast<uint64_t>(total_len);
         const uint64_t H = nheads, P = head_dim, G = ngroups, N = dstate;
@@ -238,6 +258,12 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                   make_map_3d(&m3.X, x, H * P, T, 1, xs, xs * T, 64, 1) &&
                   make_map_3d(&m3.Sprev, p.sprev, N, P, static_cast<uint64_t>(L.max_chunks) * H,
                               N * 2, P * N * 2, 64, 1);
+        if (ok && p.short_len > 0) {
+            const uint32_t R = static_cast<uint32_t>(ssd::short_scan_tile_rows(head_dim, dstate));
+            ok = make_map_plain(&ms.X, x, H * P, T, 1, xs, xs * T, R, 8, 1) &&
+                 make_map_plain(&ms.B, B, N, G, T, N * 2, bs, static_cast<uint32_t>(N), 1, 8) &&
+                 make_map_plain(&ms.C, C, N, G, T, N * 2, cs, static_cast<uint32_t>(N), 1, 8);
+        }
         if (!ok)
             return SSD_ERR_CUDA;
     }
@@ -255,7 +281,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
         return SSD_ERR_CUDA;
     if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream, pdl) != cudaSuccess)
         return SSD_ERR_CUDA;
-    if (p.short_len > 0 && ssd::launch_short_scan(p, stream, pdl) != cudaSuccess)
+    if (p.short_len > 0 && ssd::launch_short_scan(p, ms, stream, pdl) != cudaSuccess)
         return SSD_ERR_CUDA;
     if (!mark(3))
         return SSD_ERR_CUDA;

@@ -34,13 +34,22 @@ cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
 cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool programmatic);
 
 // Short sequences (<= p.short_len <= kShortLenMax tokens, including empty
-// ones): the per-token recurrence with the state in registers, y and the final
-// state written directly.  Launched after the chunk-state kernel's checks.
-// Its cost grows with the tokens while the chunked kernels spend a whole
-// 128-row block on any sequence; measured on GB300 (batches of 256 sequences,
-// 64 heads of 64 x 128) the per-token path wins up to about 8 tokens.
-constexpr int kShortLenMax = 8;
-cudaError_t launch_short_scan(const ScanParams &p, cudaStream_t stream, bool programmatic);
+// ones): the per-token recurrence on state tiles streamed through shared
+// memory, y and the final state written directly.  Launched after the
+// chunk-state kernel's checks.  Its cost grows with the tokens while the
+// chunked kernels spend a whole 128-row block, and a block state written and
+// read back, on any sequence.  Measured on GB300 with batches of 256
+// sequences, the per-token path is the faster one up to 16 tokens with 64
+// heads of 64 x 128, up to about 14 with 32 heads of 64 x 256: 12 holds both.
+constexpr int kShortLenMax = 12;
+struct ShortScanMaps {
+    CUtensorMap X;  // bf16 (H*P, T, 1), box {tile rows, 8, 1}, no swizzle
+    CUtensorMap B;  // bf16 (N, G, T), box {N, 1, 8}
+    CUtensorMap C;  // bf16 (N, G, T), box {N, 1, 8}
+};
+int short_scan_tile_rows(int P, int N);
+cudaError_t launch_short_scan(const ScanParams &p, const ShortScanMaps &maps, cudaStream_t stream,
+                              bool programmatic);
 
 // Stages 2a/2b/4: per (block, head group) C.B^T, the masked diagonal block,
 // the off-diagonal C.S_prev^T term and the D skip; writes y.

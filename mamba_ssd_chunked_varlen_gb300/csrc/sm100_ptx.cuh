@@ -109,6 +109,40 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
         : "memory");
 }
 
+// Contiguous copy global -> shared (`bytes` a multiple of 16, both addresses
+// 16-byte aligned), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Contiguous copy shared -> global (bulk-group completion), same rules.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
+// Waits until at most N committed bulk-store groups are still reading
+// shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until the committed bulk stores have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_group0()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

@@ -50,11 +50,11 @@ def test_workspace_size(lib):
     assert n1 < 33 * 16 * 64 * 256 * 6 + 64 * 1024
     assert ws(4096, 1, 16, 64, 1, 256, 128) == n1
     assert ws(4096, 2, 16, 64, 1, 256, 256) > n1          # more sequences, more chunks
-    # with several sequences, those of at most 8 tokens hold no block and at
-    # most T / 9 sequences are longer: 256 one-token sequences need
-    # ceil(256/128) + 28 = 30 blocks of scratch, not ceil(256/128) + 256
+    # with several sequences, those of at most 12 tokens hold no block and at
+    # most T / 13 sequences are longer: 256 one-token sequences need
+    # ceil(256/128) + 19 = 21 blocks of scratch, not ceil(256/128) + 256
     nd = ws(256, 256, 64, 64, 1, 128, 256)
-    assert 30 * 64 * 64 * 128 * 6 <= nd < 30 * 64 * 64 * 128 * 6 + 64 * 1024
+    assert 21 * 64 * 64 * 128 * 6 <= nd < 21 * 64 * 64 * 128 * 6 + 64 * 1024
     assert ws(0, 3, 4, 32, 1, 32, 64) > 0                 # empty sequences still need a table
     assert ws(512, 1, 4, 32, 1, 512, 64) == 0             # dstate > 256 (MAX_DSTATE)
     assert ws(512, 1, 4, 32, 1, 32, 100) == 0             # unsupported chunk size
@@ -68,8 +68,8 @@ def test_launch_count(lib):
     n = binding.ssd_scan_varlen_num_launches
     assert n(4096, 1) == 3      # block states, state passing, output
     assert n(4096, 2) == 4      # + the short-sequence kernel (a batch may hold short ones)
-    assert n(8, 1) == 4         # one sequence short enough for the per-token kernel
-    assert n(9, 1) == 3
+    assert n(12, 1) == 4        # one sequence short enough for the per-token kernel
+    assert n(13, 1) == 3
     assert n(0, 3) == 3         # empty sequences: no output kernel
     assert n(10, 0) == 0
 
