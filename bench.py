@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the Mamba-2 SSD varlen forward prefill scan on GB300.
 
-One step = one ssd_scan_varlen_fwd call (all three launches: chunk state,
-state passing, chunk scan) on the kernelindex-shaped workload: one
+One step = one ssd_scan_varlen_fwd call (all its launches: chunk state,
+state passing, chunk scan, and the short-sequence kernel when the batch has
+several sequences) on the kernelindex-shaped workload: one
 4096-token sequence, nheads=16, head_dim=64, ngroups=1, dstate=256, chunk 256
 (the head/state shape of the kernelindex "Mamba chunk scan with segsum"
 suite, whose cases are not published).  Inputs are seeded synthetic data
@@ -46,7 +47,7 @@ from mamba_ssd_chunked_varlen_gb300 import workloads as W  # noqa: E402
 METRIC = "SSD scan tokens/s and µs/call on 1 GB300; % of tensor/HBM roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
-STAGES = ("chunk_state", "state_passing", "chunk_scan")
+STAGES = ("chunk_state", "state_passing", "chunk_scan", "short_scan")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -96,47 +97,61 @@ def chunk_lengths(w) -> list:
     return out
 
 
-def work_model(w) -> dict:
+def work_model(w, short_len: int = 0) -> dict:
     """Algorithmic bytes and flops per call and per stage.
 
     Bytes are compulsory I/O only: x, dt, B, C read once, y written once,
-    pool slots read (with an initial state) and written.  Flops are the
-    chunked SSD form with exact causal triangles: C.B^T once per group,
-    the diagonal block per head, the chunk state per head, the off-diagonal
-    term per head (skipped for a first chunk without initial state).
+    pool slots read (with an initial state) and written.  Sequences of at most
+    `short_len` tokens (the library's short-sequence threshold for the call)
+    belong to the short_scan stage with all their I/O; the others to the
+    chunked stages.  Flops of the chunked stages are the chunked SSD form with
+    exact causal triangles: C.B^T once per group, the diagonal block per head,
+    the chunk state per head, the off-diagonal term per head (skipped for a
+    first chunk without initial state); of the short stage, the recurrence's
+    update and read-out (a multiply-add each per state element and token).
     """
-    T, H, P, G, N = w.total_len, w.nheads, w.head_dim, w.ngroups, w.dstate
+    H, P, G, N = w.nheads, w.head_dim, w.ngroups, w.dstate
     hinit = (np.zeros(w.batch, bool) if w.has_initial_state is None
              else w.has_initial_state.astype(bool))
-    x_b = T * H * P * 2
-    y_b = T * H * P * 2
-    dt_b = T * H * 2
-    bc_b = T * G * N * 2
+    lens = [int(L) for L in w.seq_lens]
+    short = [L <= short_len for L in lens]
+    tok = {"x": H * P * 2, "y": H * P * 2, "dt": H * 2, "bc": G * N * 2}
     slot_b = H * P * N * 4
-    pool_r = int(hinit.sum()) * slot_b
-    pool_w = w.batch * slot_b
+    T_long = sum(L for L, sh in zip(lens, short) if not sh)
+    T_short = sum(L for L, sh in zip(lens, short) if sh)
+    pool_r_long = sum(slot_b for b, sh in enumerate(short) if not sh and hinit[b])
+    pool_w_long = sum(slot_b for sh in short if not sh)
+    pool_r_short = sum(slot_b for b, sh in enumerate(short) if sh and hinit[b])
+    pool_w_short = sum(slot_b for sh in short if sh)
     f_cb = f_diag = f_state = f_off = 0
-    seq_of_chunk = []
-    for b, L in enumerate(w.seq_lens):
-        for s in range(0, int(L), w.chunk_size):
-            seq_of_chunk.append((b, min(w.chunk_size, int(L) - s), s == 0))
-    for b, l, first in seq_of_chunk:
-        tri = l * (l + 1) // 2
-        f_cb += G * tri * N * 2
-        f_diag += H * tri * P * 2
-        f_state += H * l * N * P * 2
-        if not (first and not hinit[b]):
-            f_off += H * l * N * P * 2
+    chunks = 0
+    for b, L in enumerate(lens):
+        if short[b]:
+            continue
+        for s in range(0, L, w.chunk_size):
+            l = min(w.chunk_size, L - s)
+            chunks += 1
+            tri = l * (l + 1) // 2
+            f_cb += G * tri * N * 2
+            f_diag += H * tri * P * 2
+            f_state += H * l * N * P * 2
+            if not (s == 0 and not hinit[b]):
+                f_off += H * l * N * P * 2
     stages = {
-        "chunk_state": {"bytes": x_b + bc_b + dt_b, "flops": f_state},
-        "state_passing": {"bytes": pool_r + pool_w, "flops": 0},
-        "chunk_scan": {"bytes": x_b + 2 * bc_b + dt_b + y_b, "flops": f_cb + f_diag + f_off},
+        "chunk_state": {"bytes": T_long * (tok["x"] + tok["bc"] + tok["dt"]), "flops": f_state},
+        "state_passing": {"bytes": pool_r_long + pool_w_long, "flops": 0},
+        "chunk_scan": {"bytes": T_long * (tok["x"] + 2 * tok["bc"] + tok["dt"] + tok["y"]),
+                       "flops": f_cb + f_diag + f_off},
+        "short_scan": {"bytes": T_short * (tok["x"] + 2 * tok["bc"] + tok["dt"] + tok["y"])
+                       + pool_r_short + pool_w_short,
+                       "flops": T_short * H * P * N * 4},
     }
     return {
-        "bytes": x_b + dt_b + 2 * bc_b + y_b + pool_r + pool_w,
-        "flops": f_cb + f_diag + f_state + f_off,
+        "bytes": sum(v["bytes"] for v in stages.values()) - T_long * (tok["x"] + tok["bc"] + tok["dt"]),
+        "flops": sum(v["flops"] for v in stages.values()),
         "stages": stages,
-        "chunks": len(seq_of_chunk),
+        "chunks": chunks,
+        "short_sequences": int(sum(short)),
     }
 
 
@@ -157,8 +172,9 @@ def load_peaks():
 def kernel_source_hash(stage: str) -> str:
     path = os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc", f"{stage}.cu")
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc", "sm100_ptx.cuh"),
-              os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc", "ssd_common.cuh")):
+    csrc = os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc")
+    for p in (path, os.path.join(csrc, "sm100_ptx.cuh"), os.path.join(csrc, "ssd_common.cuh"),
+              os.path.join(csrc, "ssd_device.cuh"), os.path.join(csrc, "kernels.cuh")):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -254,7 +270,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     w = W.workload(args.workload)
-    model = work_model(w)
+    model = work_model(w, pkg.ssd_scan_varlen_short_threshold(w.total_len, w.batch))
     T = w.total_len
 
     def bf(a):
@@ -352,7 +368,7 @@ def run_ours(args, rank, world, local):
     tokens_all = T * world
     value = tokens_all / (mean_ms_all * 1e-3)
 
-    # ---- per-stage attribution (stage events between the three launches)
+    # ---- per-stage attribution (stage events between the launches)
     Kp = min(K, 500)
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
            for _ in range(Kp)]

@@ -186,14 +186,16 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd_states(
     int32_t dstate, int32_t chunk_size, int32_t dt_softplus, void *workspace,
     size_t workspace_bytes, ssd_stream_t stream);
 
-/* ssd_scan_varlen_fwd with per-stage timing: `events` points to 4 CUDA events
+/* ssd_scan_varlen_fwd with per-stage timing: `events` points to 5 CUDA events
  * (cudaEvent_t, created by the caller) that are recorded on `stream` before
- * the first stage and after each of the three launches (chunk state, state
- * passing, chunk scan); cudaEventElapsedTime between consecutive events gives
- * each stage's device time.  Otherwise identical to ssd_scan_varlen_fwd
- * (same arguments, results and errors).  The records separate the launches
- * (no overlap between stages), so use it to attribute time, not to time the
- * whole call. */
+ * the first stage and after each of the four stages (chunk state, state
+ * passing, chunk scan, short sequences; a stage that does not run for these
+ * sizes gets its two events back to back); cudaEventElapsedTime between
+ * consecutive events gives each stage's device time.  Otherwise identical to
+ * ssd_scan_varlen_fwd (same arguments, results and errors).  The records
+ * separate the launches (no overlap between stages), so use it to attribute
+ * time, not to time the whole call.  With batch == 0 nothing is launched and
+ * no event is recorded. */
 SSD_API ssd_status_t ssd_scan_varlen_fwd_profiled(
     void *y, const void *x, const void *dt, const float *A, const void *B, const void *C,
     const float *D, const float *dt_bias, float *ssm_pool, const int32_t *query_start_loc,
@@ -247,6 +249,13 @@ SSD_API const char *ssd_status_string(ssd_status_t status);
 /* Number of CUDA kernels one ssd_scan_varlen_fwd call launches for these sizes
  * (0 when batch == 0).  Used to count launches when timing. */
 SSD_API int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch);
+
+/* The longest sequence (in tokens) that a call with these sizes gives to the
+ * short-sequence kernel, the per-token recurrence of the Modular page
+ * "mamba2_ssd_scan" ("Per-token recurrence"), instead of the chunked kernels:
+ * 12 when the call holds several sequences or total_len <= 12, else 0.  Both
+ * paths compute the same recurrence; this only says which kernel runs. */
+SSD_API int32_t ssd_scan_varlen_short_threshold(int64_t total_len, int32_t batch);
 
 #ifdef __cplusplus
 }

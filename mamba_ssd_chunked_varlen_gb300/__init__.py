@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     ssd_scan_varlen_fwd_noalloc,
     ssd_scan_varlen_num_launches,
     ssd_scan_varlen_read_errors,
+    ssd_scan_varlen_short_threshold,
     ssd_scan_varlen_workspace_size,
     status_string,
 )

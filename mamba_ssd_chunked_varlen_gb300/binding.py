@@ -26,6 +26,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_read_errors",
     "ssd_status_string",
     "ssd_scan_varlen_num_launches",
+    "ssd_scan_varlen_short_threshold",
 )
 
 SSD_OK = 0
@@ -83,6 +84,8 @@ def library() -> ctypes.CDLL:
     lib.ssd_status_string.argtypes = [ctypes.c_int]
     lib.ssd_scan_varlen_num_launches.restype = i32
     lib.ssd_scan_varlen_num_launches.argtypes = [i64, i32]
+    lib.ssd_scan_varlen_short_threshold.restype = i32
+    lib.ssd_scan_varlen_short_threshold.argtypes = [i64, i32]
     _lib = lib
     return lib
 
@@ -99,6 +102,10 @@ def ssd_scan_varlen_workspace_size(total_len: int, batch: int, nheads: int, head
 
 def ssd_scan_varlen_num_launches(total_len: int, batch: int) -> int:
     return int(library().ssd_scan_varlen_num_launches(total_len, batch))
+
+
+def ssd_scan_varlen_short_threshold(total_len: int, batch: int) -> int:
+    return int(library().ssd_scan_varlen_short_threshold(total_len, batch))
 
 
 def _ptr(t, what: str, dtype=None, allow_none: bool = False):
@@ -151,15 +158,15 @@ def ssd_scan_varlen_fwd_profiled(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_
                                  has_initial_state, cache_indices, *, chunk_size: int,
                                  dt_softplus: bool = True, workspace=None, stream=None,
                                  events=None) -> None:
-    """ssd_scan_varlen_fwd that also records 4 torch.cuda.Event objects around
-    the three launches (chunk state, state passing, chunk scan)."""
-    if events is None or len(events) != 4:
-        raise ValueError("events must be 4 torch.cuda.Event objects")
+    """ssd_scan_varlen_fwd that also records 5 torch.cuda.Event objects around
+    the four stages (chunk state, state passing, chunk scan, short sequences)."""
+    if events is None or len(events) != 5:
+        raise ValueError("events must be 5 torch.cuda.Event objects")
     import torch
     for e in events:
         if e.cuda_event == 0:  # torch creates the CUDA event lazily, on first record
             e.record(torch.cuda.current_stream() if stream is None else stream)
-    handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    handles = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     st = library().ssd_scan_varlen_fwd_profiled(
         *_fwd_args(y, x, dt, A, B, C, D, dt_bias, ssm_pool, query_start_loc, has_initial_state,
                    cache_indices, chunk_size, dt_softplus, workspace, stream), handles)

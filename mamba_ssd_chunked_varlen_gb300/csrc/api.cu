@@ -139,6 +139,11 @@ size_t ssd_scan_varlen_workspace_size(int64_t total_len, int32_t batch, int32_t 
                           ssd::block_tokens(chunk_size), short_len_of(total_len, batch)).total;
 }
 
+int32_t ssd_scan_varlen_short_threshold(int64_t total_len, int32_t batch)
+{
+    return batch > 0 ? short_len_of(total_len, batch) : 0;
+}
+
 int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
 {
     if (batch <= 0)
@@ -281,9 +286,11 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
         return SSD_ERR_CUDA;
     if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream, pdl) != cudaSuccess)
         return SSD_ERR_CUDA;
+    if (!mark(3))
+        return SSD_ERR_CUDA;
     if (p.short_len > 0 && ssd::launch_short_scan(p, ms, stream, pdl) != cudaSuccess)
         return SSD_ERR_CUDA;
-    if (!mark(3))
+    if (!mark(4))
         return SSD_ERR_CUDA;
     return SSD_OK;
 }
@@ -379,7 +386,7 @@ ssd_status_t ssd_scan_varlen_fwd_profiled(
 {
     if (!events)
         return SSD_ERR_INVALID_ARG;
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < 5; ++k)
         if (!events[k])
             return SSD_ERR_INVALID_ARG;
     const ssd::StateIO io{ssm_pool, cache_indices, max_slots, nullptr, nullptr, 0};

@@ -89,7 +89,7 @@ struct TokenStrides {
 };
 
 // The whole scan (argument checks, tensor maps, the three launches) on a
-// caller-provided scratch buffer; `events` (4 CUDA events) may be null.
+// caller-provided scratch buffer; `events` (5 CUDA events) may be null.
 ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
                        const void *C, const float *D, const float *dt_bias, const StateIO &io,
                        const int32_t *query_start_loc, const uint8_t *has_initial_state,

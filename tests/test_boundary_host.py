@@ -74,6 +74,19 @@ def test_launch_count(lib):
     assert n(10, 0) == 0
 
 
+def test_short_threshold(lib):
+    s = binding.ssd_scan_varlen_short_threshold
+    assert s(4096, 1) == 0      # one long sequence: the chunked kernels only
+    assert s(12, 1) == 12 and s(13, 1) == 0
+    assert s(4096, 2) == 12     # several sequences: those of <= 12 tokens
+    assert s(0, 3) == 12
+    assert s(10, 0) == 0
+    # the launch count follows the threshold
+    n = binding.ssd_scan_varlen_num_launches
+    for T, b in [(4096, 1), (12, 1), (13, 1), (4096, 2), (0, 3)]:
+        assert n(T, b) == 2 + (T > 0) + (s(T, b) > 0)
+
+
 def _call(lib, **over):
     args = dict(y=1 << 12, x=1 << 12, dt=1 << 12, A=1 << 12, B=1 << 12, C=1 << 12, D=None,
                 dt_bias=None, pool=1 << 12, qsl=1 << 12, hinit=None, cidx=1 << 12,
