@@ -163,6 +163,25 @@ def test_bad_query_start_loc_sets_flag_and_writes_nothing():
     assert torch.isnan(y.float()).all()  # y untouched (was NaN-filled)
 
 
+@pytest.mark.parametrize("qsl", [[0, 300], [1, 400], [0, 500]])
+def test_bad_query_start_loc_one_sequence(qsl):
+    """One sequence (whose blocks the kernels place before reading
+    query_start_loc): a query_start_loc that does not span [0, total_len]
+    still sets the flag and writes nothing."""
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    w = W.make_workload("badqsl1", [400], 4, 64, 1, 64, 128, max_slots=2, seed=47,
+                        has_init_p=1.0)
+    d = to_device(w)
+    d["query_start_loc"] = torch.tensor(qsl, dtype=torch.int32, device="cuda")
+    pool_before = d["ssm_pool"].clone()
+    y, pool, _, ws = run_cuda(w, dev=d)
+    flags = pkg.ssd_scan_varlen_read_errors(ws)
+    assert flags & pkg.binding.DEVERR_BAD_QUERY_START_LOC
+    assert not flags & pkg.binding.DEVERR_TIMEOUT
+    assert torch.equal(pool_before, pool)
+    assert torch.isnan(y.float()).all()
+
+
 # ---------------------------------------------------------------- routing, bit-exact
 
 def test_permuting_the_batch_is_bit_exact():
