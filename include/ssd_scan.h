@@ -247,7 +247,10 @@ SSD_API ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stre
 SSD_API const char *ssd_status_string(ssd_status_t status);
 
 /* Number of CUDA kernels one ssd_scan_varlen_fwd call launches for these sizes
- * (0 when batch == 0).  Used to count launches when timing. */
+ * (0 when batch == 0): chunk state and state passing, chunk scan when
+ * total_len > 0, the short-sequence kernel when the call may hold short
+ * sequences, and a block-map kernel for batches of more than 512 sequences.
+ * Used to count launches when timing. */
 SSD_API int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch);
 
 /* The longest sequence (in tokens) that a call with these sizes gives to the

@@ -148,7 +148,8 @@ int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
 {
     if (batch <= 0)
         return 0;
-    return 2 + (total_len > 0 ? 1 : 0) + (short_path(total_len, batch) ? 1 : 0);
+    return 2 + (total_len > 0 ? 1 : 0) + (short_path(total_len, batch) ? 1 : 0) +
+           (batch > ssd::kMapBatchMax ? 1 : 0);
 }
 
 }  // extern "C"
@@ -242,6 +243,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);
     p.short_list = reinterpret_cast<ssd::SeqRec *>(ws + L.short_list);
     p.long_list = reinterpret_cast<ssd::SeqRec *>(ws + L.long_list);
+    p.table = batch > ssd::kMapBatchMax ? reinterpret_cast<ssd::BlockEntry *>(ws + L.table) : nullptr;
     p.decay = reinterpret_cast<float *>(ws + L.decay);
     p.schunk = reinterpret_cast<float *>(ws + L.schunk);
     p.sprev = reinterpret_cast<__nv_bfloat16 *>(ws + L.sprev);
@@ -280,7 +282,10 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                cudaEventRecord(static_cast<cudaEvent_t>(events[k]), stream) == cudaSuccess;
     };
     const bool pdl = events == nullptr;
-    if (!mark(0) || ssd::launch_chunk_state(p, m1, stream) != cudaSuccess || !mark(1))
+    // large batches: the block map first, the chunk-state kernel its dependent
+    const bool mapped = p.table != nullptr;
+    if (!mark(0) || (mapped && ssd::launch_block_map(p, stream) != cudaSuccess) ||
+        ssd::launch_chunk_state(p, m1, stream, mapped && pdl) != cudaSuccess || !mark(1))
         return SSD_ERR_CUDA;
     if (ssd::launch_state_passing(p, stream, pdl) != cudaSuccess || !mark(2))
         return SSD_ERR_CUDA;

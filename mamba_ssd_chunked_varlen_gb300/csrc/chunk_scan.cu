@@ -174,7 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmX);
         ptx::prefetch_tensormap(&tmS);
     }
-    const BlockInfo bi = map_block<kThreads>(p, blk, scratch, nullptr);
+    // with the block table the block-map kernel has completed (the chunk-state
+    // CTAs read it before letting later kernels launch)
+    const BlockInfo bi = p.table != nullptr ? lookup_block(p, blk)
+                                            : map_block<kThreads>(p, blk, scratch, nullptr);
     // Every CTA waits for the state-passing grid before it leaves (those without
     // an entering state would not otherwise), so that this grid completes only
     // after its predecessors and a dependent launch may rely on all of them.

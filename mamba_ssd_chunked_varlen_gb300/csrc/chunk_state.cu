@@ -66,6 +66,66 @@ __host__ __device__ inline K1Layout k1_layout(int NP, int n_mtiles, int HB)
     return L;
 }
 
+// The per-call bookkeeping, by one CTA of kThreads threads after its block
+// map (which wrote seq_first): the bad-slot checks, the two work lists of
+// sequence records (short ones for the short-sequence kernel, the others for
+// state passing) and the header (valid flag, block count).  `scratch` is the
+// block map's shared ints; 38 and 39 are used here.
+__device__ void call_bookkeeping(const ScanParams &p, const BlockInfo &bi, int32_t *scratch)
+{
+    const int tid = threadIdx.x;
+    if (p.pool != nullptr)
+        for (int b = tid; b < p.batch; b += kThreads)
+            if (static_cast<int64_t>(p.cache_idx[b]) >= p.max_slots)
+                record_error(p.hdr, kErrBadSlot);
+    int32_t *s_count = scratch + 38, *l_count = scratch + 39;   // past map_block's ints
+    if (tid == 0) {
+        *s_count = 0;
+        *l_count = 0;
+    }
+    __syncthreads();   // also orders map_block's seq_first writes before the reads
+    if (bi.valid)
+        for (int b = tid; b < p.batch; b += kThreads) {
+            SeqRec r;
+            r.t0 = p.qsl[b];
+            r.len = p.qsl[b + 1] - r.t0;
+            r.c_begin = p.seq_first[b];
+            r.c_end = p.seq_first[b + 1];
+            r.init = seq_init_index(p, b);
+            r.fin = seq_final_index(p, b);
+            if (r.len <= p.short_len)
+                p.short_list[atomicAdd(s_count, 1)] = r;
+            else
+                p.long_list[atomicAdd(l_count, 1)] = r;
+        }
+    __syncthreads();
+    if (tid == 0) {
+        p.hdr->n_short = *s_count;
+        p.hdr->n_long = *l_count;
+        if (!bi.valid)
+            record_error(p.hdr, kErrBadQsl);
+        p.hdr->valid = bi.valid;
+        p.hdr->nchunks = bi.valid ? bi.total : 0;
+        __threadfence();
+    }
+}
+
+// Batches of more than kMapBatchMax sequences: one CTA maps every block once
+// into the block table (and does the bookkeeping); the block kernels, launched
+// as its programmatic dependents, look their block up instead of scanning
+// query_start_loc each.
+__global__ void __launch_bounds__(kThreads) block_map_kernel(ScanParams p)
+{
+    __shared__ int32_t scratch[64];
+    // the chunk-state kernel may start launching; it waits for this grid
+    pdl_launch_dependents();
+    if (threadIdx.x == 0)
+        p.hdr->errors = 0u;
+    // a block index past every block: the scan only writes the tables
+    const BlockInfo bi = map_block<kThreads>(p, int64_t(1) << 62, scratch, p.seq_first, p.table);
+    call_bookkeeping(p, bi, scratch);
+}
+
 __global__ void __launch_bounds__(kThreads)
     chunk_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
                        ScanParams p, int HB, int NP, int n_mtiles, uint32_t tmem_cols)
@@ -103,52 +163,21 @@ __global__ void __launch_bounds__(kThreads)
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmX);
     }
-    if (leader && tid == 0)
-        p.hdr->errors = 0u;
-    const BlockInfo bi = map_block<kThreads>(p, blk, scratch, leader ? p.seq_first : nullptr);
-    if (leader) {
-        if (p.pool != nullptr)
-            for (int b = tid; b < p.batch; b += kThreads)
-                if (static_cast<int64_t>(p.cache_idx[b]) >= p.max_slots)
-                    record_error(p.hdr, kErrBadSlot);
-        // the work lists: short sequences for the short-sequence kernel, the
-        // others for state passing
-        {
-            int32_t *s_count = scratch + 38, *l_count = scratch + 39;   // past map_block's ints
-            if (tid == 0) {
-                *s_count = 0;
-                *l_count = 0;
-            }
-            __syncthreads();   // also orders map_block's seq_first writes before the reads
-            if (bi.valid)
-                for (int b = tid; b < p.batch; b += kThreads) {
-                    SeqRec r;
-                    r.t0 = p.qsl[b];
-                    r.len = p.qsl[b + 1] - r.t0;
-                    r.c_begin = p.seq_first[b];
-                    r.c_end = p.seq_first[b + 1];
-                    r.init = seq_init_index(p, b);
-                    r.fin = seq_final_index(p, b);
-                    if (r.len <= p.short_len)
-                        p.short_list[atomicAdd(s_count, 1)] = r;
-                    else
-                        p.long_list[atomicAdd(l_count, 1)] = r;
-                }
-            __syncthreads();
-            if (tid == 0) {
-                p.hdr->n_short = *s_count;
-                p.hdr->n_long = *l_count;
-            }
-        }
-        if (tid == 0) {
-            if (!bi.valid)
-                record_error(p.hdr, kErrBadQsl);
-            p.hdr->valid = bi.valid;
-            p.hdr->nchunks = bi.valid ? bi.total : 0;
-            __threadfence();
-        }
+    BlockInfo bi;
+    if (p.table != nullptr) {
+        // the block-map kernel has mapped every block (and done the bookkeeping)
+        pdl_wait();
+        bi = lookup_block(p, blk);
+    } else {
+        if (leader && tid == 0)
+            p.hdr->errors = 0u;
+        bi = map_block<kThreads>(p, blk, scratch, leader ? p.seq_first : nullptr);
+        if (leader)
+            call_bookkeeping(p, bi, scratch);
     }
     // the state-passing kernel may start launching; it waits for this grid
+    // (with the block table, only once this CTA has read it, so that every
+    // later kernel finds the block-map kernel complete)
     pdl_launch_dependents();
     if (!bi.valid || bi.seq < 0)
         return;
@@ -392,17 +421,31 @@ K1Config chunk_state_config(int H, int G, int P, int N)
     return c;
 }
 
+cudaError_t launch_block_map(const ScanParams &p, cudaStream_t stream)
+{
+    block_map_kernel<<<1, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
-                               cudaStream_t stream)
+                               cudaStream_t stream, bool programmatic)
 {
     const K1Config c = chunk_state_config(p.H, p.G, p.P, p.N);
     cudaError_t e = ensure_max_smem(reinterpret_cast<const void *>(chunk_state_kernel), s_smem_configured);
     if (e != cudaSuccess)
         return e;
-    dim3 grid(p.max_chunks, p.H / c.HB);
-    chunk_state_kernel<<<grid, kThreads, c.smem, stream>>>(maps.B, maps.X, p, c.HB, c.NP,
-                                                           c.n_mtiles, c.tmem_cols);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.max_chunks, p.H / c.HB);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = c.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chunk_state_kernel, maps.B, maps.X, p, c.HB, c.NP, c.n_mtiles,
+                              c.tmem_cols);
 }
 
 }  // namespace ssd

@@ -26,7 +26,12 @@ struct K1Config {
 };
 K1Config chunk_state_config(int H, int G, int P, int N);
 cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool programmatic);
+
+// Batches of more than kMapBatchMax sequences: one CTA scans query_start_loc
+// once, writes the block table and does the per-call bookkeeping; launched
+// before the chunk-state kernel, which then runs as its programmatic dependent.
+cudaError_t launch_block_map(const ScanParams &p, cudaStream_t stream);
 
 // Stage 3: inter-block state passing; writes the state entering every block
 // and the final state of every sequence into its pool slot.  `programmatic`:

@@ -31,7 +31,18 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 // Byte offsets of the workspace regions; every region is 256-byte aligned.
 struct WsLayout {
     int64_t max_chunks;
-    size_t header, seq_first, short_list, long_list, decay, schunk, sprev, total;
+    size_t header, seq_first, short_list, long_list, table, decay, schunk, sprev, total;
+};
+
+// Batches of more sequences than this map their blocks once, in a kernel of
+// their own that writes a block table, instead of in every CTA (a scan of
+// query_start_loc per CTA costs a round per 512 sequences).
+constexpr int32_t kMapBatchMax = 512;
+
+// Where a block lies, as the block table records it.
+struct alignas(16) BlockEntry {
+    int32_t seq, t0, len;
+    int32_t flags;   // 1: the sequence's first block, 2: its last
 };
 
 // One sequence of a work list, resolved by the chunk-state kernel's
@@ -82,6 +93,8 @@ __host__ __device__ inline WsLayout ws_layout(int64_t T, int32_t batch, int32_t 
     off = align256(off + sizeof(SeqRec) * static_cast<size_t>(batch));
     L.long_list = off;
     off = align256(off + sizeof(SeqRec) * static_cast<size_t>(batch));
+    L.table = off;
+    off = align256(off + (batch > kMapBatchMax ? sizeof(BlockEntry) * mc : 0));
     L.decay = off;
     off = align256(off + sizeof(float) * mc * H);
     L.schunk = off;
@@ -127,6 +140,8 @@ struct ScanParams {
     int32_t *seq_first;   // (batch + 1): first block of each sequence, then the total
     SeqRec *short_list;   // the short sequences (hdr->n_short of them)
     SeqRec *long_list;    // the other sequences (hdr->n_long), state passing's list
+    BlockEntry *table;    // per block, for batches above kMapBatchMax; else null (each
+                          // CTA maps its own block)
     float *decay;         // [block][head] exp(sum of A*dt over the block)
     float *schunk;        // [block][head][P][N] block states (zero initial state)
     __nv_bfloat16 *sprev; // [block][head][P][N] state entering each block (bf16 operand)

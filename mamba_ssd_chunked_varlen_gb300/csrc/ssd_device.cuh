@@ -137,12 +137,13 @@ struct BlockInfo {
 // Maps block `blk` by scanning query_start_loc.  Called by every thread of a
 // CTA of kThreads threads (kThreads a multiple of 32, <= 1024); uses `scratch`
 // (ints 0-36 of shared memory).  When `seq_first` is non-null the CTA also
-// writes every sequence's first block index there (and the total at [batch]).
+// writes every sequence's first block index there (and the total at [batch]),
+// and, when `table` is non-null, every block's entry.
 // One pass over query_start_loc per kThreads sequences: the checks of its
 // first and last entries ride along with the loads of the scan.
 template <int kThreads>
 __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratch,
-                               int32_t *seq_first)
+                               int32_t *seq_first, BlockEntry *table = nullptr)
 {
     constexpr int kWarps = kThreads / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -180,6 +181,12 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
         if (b < p.batch) {
             if (seq_first)
                 seq_first[b] = first;
+            // (a query_start_loc that fails the checks may give any count: the
+            // entries stay inside the table, which is then not used)
+            if (table && first >= 0)
+                for (int32_t k = 0; k < n && first + k < p.max_chunks; ++k)
+                    table[first + k] = BlockEntry{b, start + k * p.Q, min(p.Q, len - k * p.Q),
+                                                  (k == 0 ? 1 : 0) | (k == n - 1 ? 2 : 0)};
             if (blk >= first && blk < first + n) {
                 const int32_t k = static_cast<int32_t>(blk - first);
                 s_res[0] = b;
@@ -204,6 +211,23 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
     bi.len = mine ? s_res[2] : 0;
     bi.first = mine ? s_res[3] : 0;
     bi.last = mine ? s_res[4] : 0;
+    return bi;
+}
+
+// Block `blk` from the block table (the block-map kernel's output; read only
+// after that kernel has completed).
+__device__ __forceinline__ BlockInfo lookup_block(const ScanParams &p, int64_t blk)
+{
+    BlockInfo bi;
+    bi.valid = p.hdr->valid;
+    bi.total = p.hdr->nchunks;
+    const bool mine = bi.valid && blk < bi.total;
+    const BlockEntry e = mine ? p.table[blk] : BlockEntry{-1, 0, 0, 0};
+    bi.seq = e.seq;
+    bi.t0 = e.t0;
+    bi.len = e.len;
+    bi.first = e.flags & 1;
+    bi.last = (e.flags >> 1) & 1;
     return bi;
 }
 

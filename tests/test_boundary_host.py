@@ -72,6 +72,8 @@ def test_launch_count(lib):
     assert n(13, 1) == 3
     assert n(0, 3) == 3         # empty sequences: no output kernel
     assert n(10, 0) == 0
+    assert n(5000, 512) == 4    # up to 512 sequences every CTA maps its own block
+    assert n(5000, 513) == 5    # beyond, a block-map kernel writes a block table
 
 
 def test_short_threshold(lib):

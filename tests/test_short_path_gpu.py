@@ -58,3 +58,61 @@ def test_short_sequence_alone_equals_in_batch():
         assert torch.equal(y1.view(torch.int16), y_all[t0:t1].view(torch.int16)), f"seq {b}: y"
         s = int(w.cache_indices[b])
         assert torch.equal(pool1[s].view(torch.int32), pool_all[s].view(torch.int32)), f"seq {b}: state"
+
+
+def _split_runs(w, cut):
+    """The workload as two calls: sequences [0, cut) and [cut, batch)."""
+    out = []
+    for lo, hi in ((0, cut), (cut, w.batch)):
+        t0, t1 = int(w.query_start_loc[lo]), int(w.query_start_loc[hi])
+        out.append(dataclasses.replace(
+            w, x=w.x[t0:t1], dt=w.dt[t0:t1], B=w.B[t0:t1], C=w.C[t0:t1],
+            query_start_loc=(w.query_start_loc[lo:hi + 1] - t0).astype(np.int32),
+            has_initial_state=w.has_initial_state[lo:hi],
+            cache_indices=w.cache_indices[lo:hi]))
+    return out
+
+
+def test_large_batch_block_table():
+    """More than 512 sequences: a block-map kernel writes a block table that the
+    block kernels read.  Every sequence must give the bits it gives in a call
+    of at most 512 sequences (where each CTA maps its own block), and the whole
+    must match the oracle."""
+    rng = np.random.default_rng(71)
+    lens = rng.choice([0, 1, 3, 7, 12, 13, 40, 128, 129, 300], size=700)
+    w = W.make_workload("big_batch", [int(v) for v in lens], 4, 32, 2, 32, 64,
+                        max_slots=720, seed=72, has_init_p=0.6)
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    assert pkg.ssd_scan_varlen_num_launches(w.total_len, w.batch) == 5
+    y, pool, _, ws = run_cuda(w)
+    assert pkg.ssd_scan_varlen_read_errors(ws) == 0
+    y_ref, pool_ref = recurrence.run_workload(w)
+    check_y(y_to_f64(y), y_ref, what="700 sequences")
+    check_slots(pool.cpu().numpy(), pool_ref, w.ssm_pool, w, what="700 sequences")
+    # the same sequences in two calls of 350
+    parts = _split_runs(w, 350)
+    w1 = parts[0]
+    y1, pool1, _, _ = run_cuda(w1)
+    w2 = dataclasses.replace(parts[1], ssm_pool=pool1.cpu().numpy())
+    y2, pool2, _, _ = run_cuda(w2)
+    t_cut = int(w.query_start_loc[350])
+    assert torch.equal(y[:t_cut].view(torch.int16), y1.view(torch.int16))
+    assert torch.equal(y[t_cut:].view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(pool.view(torch.int32), pool2.view(torch.int32))
+
+
+def test_large_batch_bad_query_start_loc():
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    from helpers import to_device
+    w = W.make_workload("big_bad", [5] * 600, 2, 32, 1, 32, 64, max_slots=600, seed=73)
+    d = to_device(w)
+    qsl = w.query_start_loc.copy()
+    qsl[300] = qsl[301] + 1          # a negative length
+    d["query_start_loc"] = torch.from_numpy(qsl).cuda()
+    pool_before = d["ssm_pool"].clone()
+    y, pool, _, ws = run_cuda(w, dev=d)
+    flags = pkg.ssd_scan_varlen_read_errors(ws)
+    assert flags & pkg.binding.DEVERR_BAD_QUERY_START_LOC
+    assert not flags & pkg.binding.DEVERR_TIMEOUT
+    assert torch.equal(pool_before, pool)
+    assert torch.isnan(y.float()).all()
