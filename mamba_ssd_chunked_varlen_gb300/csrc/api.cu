@@ -238,6 +238,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.Q = Qb;
     p.dt_softplus = dt_softplus ? 1 : 0;
     p.short_len = short_len_of(total_len, batch);
+    p.finish_single = batch > 1 ? 1 : 0;
     p.max_chunks = static_cast<int32_t>(L.max_chunks);
     p.hdr = reinterpret_cast<ssd::WsHeader *>(ws + L.header);
     p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);

@@ -93,9 +93,10 @@ __device__ void call_bookkeeping(const ScanParams &p, const BlockInfo &bi, int32
             r.c_end = p.seq_first[b + 1];
             r.init = seq_init_index(p, b);
             r.fin = seq_final_index(p, b);
+            // a sequence of one block may be finished by the chunk-state kernel
             if (r.len <= p.short_len)
                 p.short_list[atomicAdd(s_count, 1)] = r;
-            else
+            else if (!p.finish_single || r.c_end - r.c_begin > 1)
                 p.long_list[atomicAdd(l_count, 1)] = r;
         }
     __syncthreads();
@@ -126,7 +127,12 @@ __global__ void __launch_bounds__(kThreads) block_map_kernel(ScanParams p)
     call_bookkeeping(p, bi, scratch);
 }
 
-__global__ void __launch_bounds__(kThreads)
+// kFinishSingle: a sequence's only block is finished here (batches of several
+// sequences); without it every block state goes to the state-passing kernel
+// and the kernel keeps to 64 registers, so that two state-passing CTAs wait
+// beside it.
+template <bool kFinishSingle>
+__global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
     chunk_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
                        ScanParams p, int HB, int NP, int n_mtiles, uint32_t tmem_cols)
 {
@@ -352,28 +358,86 @@ __global__ void __launch_bounds__(kThreads)
 
     if (!failed) {
         // ---- epilogue: S^T tile [n][(h,p)] -> S_c[blk][h][p][n] ----
+        // A sequence's only block is finished here instead of in the state-
+        // passing kernel, with the same arithmetic: the entering state is the
+        // initial state (its bf16 copy goes to S_prev for the chunk-scan
+        // kernel), the final state decay * initial + S_c goes to its slot.
+        // The initial state is loaded before the MMAs are waited for.
+        const bool single = kFinishSingle && bi.first && bi.last;
+        const int64_t init_i = single ? seq_init_index(p, bi.seq) : -1;
+        const int64_t fin_i = single ? seq_final_index(p, bi.seq) : -1;
         const int q = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
-        const int ncols = NP / 4;
+        const int ncols = NP / 4;                // <= 64: at most 4 chunks of 16
         for (int mt = 0; mt < n_mtiles && !failed; ++mt) {
-            if (!ptx::mbar_wait(bar_mma + mt, 0, kWaitTimeoutNs)) {
-                failed = true;
-                break;
-            }
-            ptx::tc_fence_after_sync();
             const int n = mt * 128 + q * 32 + lane;
+            if (!single) {
+                if (!ptx::mbar_wait(bar_mma + mt, 0, kWaitTimeoutNs)) {
+                    failed = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
 #pragma unroll 1
-            for (int c = cq * ncols; c < (cq + 1) * ncols; c += 16) {
-                float v[16];
-                ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * NP + c, v);
-                if (n < p.N && c < width) {
-                    // 16 columns never straddle two heads (head_dim % 16 == 0); a
-                    // warp writes 32 consecutive n of one p: 128 contiguous bytes
-                    const int hh = c / p.P, p0 = c % p.P;
-                    float *dst = p.schunk +
-                                 ((static_cast<int64_t>(blk) * p.H + h0 + hh) * p.P + p0) * p.N + n;
+                for (int c = cq * ncols; c < (cq + 1) * ncols; c += 16) {
+                    float v[16];
+                    ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * NP + c, v);
+                    if (n < p.N && c < width) {
+                        // 16 columns never straddle two heads (head_dim % 16 == 0); a
+                        // warp writes 32 consecutive n of one p: 128 contiguous bytes
+                        const int hh = c / p.P, p0 = c % p.P;
+                        float *dst = p.schunk +
+                                     ((static_cast<int64_t>(blk) * p.H + h0 + hh) * p.P + p0) * p.N + n;
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        dst[static_cast<int64_t>(k) * p.N] = v[k];
+                        for (int k = 0; k < 16; ++k)
+                            dst[static_cast<int64_t>(k) * p.N] = v[k];
+                    }
+                }
+                continue;
+            }
+            if constexpr (kFinishSingle) {
+                // the initial state of all this thread's columns is loaded
+                // before the MMAs are waited for
+                float iv[4][16];
+                if (init_i >= 0) {
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int c = cq * ncols + ci * 16;
+                        if (ci * 16 < ncols && n < p.N && c < width) {
+                            const int64_t e =
+                                (static_cast<int64_t>(h0 + c / p.P) * p.P + c % p.P) * p.N + n;
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                iv[ci][k] = load_init1(p, init_i + e + static_cast<int64_t>(k) * p.N);
+                        }
+                    }
+                }
+                if (!ptx::mbar_wait(bar_mma + mt, 0, kWaitTimeoutNs)) {
+                    failed = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) {
+                    if (ci * 16 >= ncols)
+                        break;
+                    const int c = cq * ncols + ci * 16;
+                    float v[16];
+                    ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * NP + c, v);
+                    if (n < p.N && c < width) {
+                        const int hh = c / p.P, p0 = c % p.P;
+                        const int64_t row = (static_cast<int64_t>(blk) * p.H + h0 + hh) * p.P + p0;
+                        const float d = expf(sAcum[hh * kRows + len - 1]);
+                        const int64_t e = (static_cast<int64_t>(h0 + hh) * p.P + p0) * p.N + n;
+                        __nv_bfloat16 *sp = p.sprev + row * p.N + n;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float s0 = init_i >= 0 ? iv[ci][k] : 0.f;
+                            if (init_i >= 0)
+                                sp[static_cast<int64_t>(k) * p.N] = __float2bfloat16_rn(s0);
+                            if (fin_i >= 0)
+                                store_final1(p, fin_i + e + static_cast<int64_t>(k) * p.N,
+                                             fmaf(d, s0, v[k]));
+                        }
+                    }
                 }
             }
         }
@@ -391,7 +455,7 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-SmemOptIn s_smem_configured;
+SmemOptIn s_smem_configured, s_smem_configured_single;
 
 }  // namespace
 
@@ -431,7 +495,11 @@ cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
                                cudaStream_t stream, bool programmatic)
 {
     const K1Config c = chunk_state_config(p.H, p.G, p.P, p.N);
-    cudaError_t e = ensure_max_smem(reinterpret_cast<const void *>(chunk_state_kernel), s_smem_configured);
+    const void *kernel = p.finish_single
+                             ? reinterpret_cast<const void *>(chunk_state_kernel<true>)
+                             : reinterpret_cast<const void *>(chunk_state_kernel<false>);
+    cudaError_t e = ensure_max_smem(kernel, p.finish_single ? s_smem_configured_single
+                                                            : s_smem_configured);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -444,8 +512,11 @@ cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
     attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_state_kernel, maps.B, maps.X, p, c.HB, c.NP, c.n_mtiles,
-                              c.tmem_cols);
+    if (p.finish_single)
+        return cudaLaunchKernelEx(&cfg, chunk_state_kernel<true>, maps.B, maps.X, p, c.HB, c.NP,
+                                  c.n_mtiles, c.tmem_cols);
+    return cudaLaunchKernelEx(&cfg, chunk_state_kernel<false>, maps.B, maps.X, p, c.HB, c.NP,
+                              c.n_mtiles, c.tmem_cols);
 }
 
 }  // namespace ssd

@@ -132,6 +132,8 @@ struct ScanParams {
     int32_t Q;            // tokens per block (block_tokens of the chunk size)
     int64_t max_slots;
     int32_t dt_softplus;
+    int32_t finish_single;   // 1: the chunk-state kernel finishes one-block sequences
+                             // (their final and entering states; state passing skips them)
     int32_t short_len;    // sequences of at most this many tokens go to the short-sequence
                           // kernel (the chunked kernels skip them); 0: none
     int32_t max_chunks;   // upper bound on the number of blocks

@@ -121,6 +121,28 @@ __device__ __forceinline__ void store_final4(const ScanParams &p, int64_t i, flo
     }
 }
 
+// One state element from the initial-state storage, widened to fp32.
+__device__ __forceinline__ float load_init1(const ScanParams &p, int64_t i)
+{
+    if (p.pool == nullptr)
+        return p.init_states[i];
+    if (!p.pool_bf16)
+        return static_cast<const float *>(p.pool)[i];
+    return __bfloat162float(static_cast<const __nv_bfloat16 *>(p.pool)[i]);
+}
+
+// One final-state element into its storage (bf16 storage rounds to nearest
+// even).
+__device__ __forceinline__ void store_final1(const ScanParams &p, int64_t i, float v)
+{
+    if (p.pool == nullptr)
+        p.final_states[i] = v;
+    else if (!p.pool_bf16)
+        static_cast<float *>(p.pool)[i] = v;
+    else
+        static_cast<__nv_bfloat16 *>(p.pool)[i] = __float2bfloat16_rn(v);
+}
+
 // ---------------------------------------------------------------- block map
 // Where a block (at most `blk_len` tokens of one sequence, aligned to the
 // sequence start) lies: blocks are numbered sequence after sequence.
