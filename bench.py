@@ -104,7 +104,8 @@ def work_model(w, short_len: int = 0) -> dict:
     pool slots read (with an initial state) and written.  Sequences of at most
     `short_len` tokens (the library's short-sequence threshold for the call)
     belong to the short_scan stage with all their I/O; the others to the
-    chunked stages.  Flops of the chunked stages are the chunked SSD form with
+    chunked stages, the slots of one-block sequences (in calls of several
+    sequences) to chunk_state, which finishes them.  Flops of the chunked stages are the chunked SSD form with
     exact causal triangles: C.B^T once per group, the diagonal block per head,
     the chunk state per head, the off-diagonal term per head (skipped for a
     first chunk without initial state); of the short stage, the recurrence's
@@ -119,8 +120,14 @@ def work_model(w, short_len: int = 0) -> dict:
     slot_b = H * P * N * 4
     T_long = sum(L for L, sh in zip(lens, short) if not sh)
     T_short = sum(L for L, sh in zip(lens, short) if sh)
-    pool_r_long = sum(slot_b for b, sh in enumerate(short) if not sh and hinit[b])
-    pool_w_long = sum(slot_b for sh in short if not sh)
+    # in calls of several sequences the chunk-state kernel finishes one-block
+    # sequences (their slot traffic is its); state passing takes the others
+    Qb = min(w.chunk_size, 128)
+    one_block = [not sh and w.batch > 1 and L <= Qb for L, sh in zip(lens, short)]
+    pool_r_one = sum(slot_b for b, o in enumerate(one_block) if o and hinit[b])
+    pool_w_one = sum(slot_b for o in one_block if o)
+    pool_r_long = sum(slot_b for b, sh in enumerate(short) if not sh and hinit[b]) - pool_r_one
+    pool_w_long = sum(slot_b for sh in short if not sh) - pool_w_one
     pool_r_short = sum(slot_b for b, sh in enumerate(short) if sh and hinit[b])
     pool_w_short = sum(slot_b for sh in short if sh)
     f_cb = f_diag = f_state = f_off = 0
@@ -138,7 +145,8 @@ def work_model(w, short_len: int = 0) -> dict:
             if not (s == 0 and not hinit[b]):
                 f_off += H * l * N * P * 2
     stages = {
-        "chunk_state": {"bytes": T_long * (tok["x"] + tok["bc"] + tok["dt"]), "flops": f_state},
+        "chunk_state": {"bytes": T_long * (tok["x"] + tok["bc"] + tok["dt"]) + pool_r_one + pool_w_one,
+                        "flops": f_state},
         "state_passing": {"bytes": pool_r_long + pool_w_long, "flops": 0},
         "chunk_scan": {"bytes": T_long * (tok["x"] + 2 * tok["bc"] + tok["dt"] + tok["y"]),
                        "flops": f_cb + f_diag + f_off},
@@ -147,7 +155,8 @@ def work_model(w, short_len: int = 0) -> dict:
                        "flops": T_short * H * P * N * 4},
     }
     return {
-        "bytes": sum(v["bytes"] for v in stages.values()) - T_long * (tok["x"] + tok["bc"] + tok["dt"]),
+        "bytes": (sum(v["bytes"] for v in stages.values())
+                  - T_long * (tok["x"] + tok["bc"] + tok["dt"])),
         "flops": sum(v["flops"] for v in stages.values()),
         "stages": stages,
         "chunks": chunks,
