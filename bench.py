@@ -97,7 +97,7 @@ def chunk_lengths(w) -> list:
     return out
 
 
-def work_model(w, short_len: int = 0) -> dict:
+def work_model(w, short_len: int = 0, fused_walk: bool = False) -> dict:
     """Algorithmic bytes and flops per call and per stage.
 
     Bytes are compulsory I/O only: x, dt, B, C read once, y written once,
@@ -105,7 +105,10 @@ def work_model(w, short_len: int = 0) -> dict:
     `short_len` tokens (the library's short-sequence threshold for the call)
     belong to the short_scan stage with all their I/O; the others to the
     chunked stages, the slots of one-block sequences (in calls of several
-    sequences) to chunk_state, which finishes them.  Flops of the chunked stages are the chunked SSD form with
+    sequences) to chunk_state, which finishes them.  With `fused_walk` (the
+    library runs the chunk states and the state recurrence as one kernel, timed
+    as the chunk_state stage) every slot of the chunked path is chunk_state's.
+    Flops of the chunked stages are the chunked SSD form with
     exact causal triangles: C.B^T once per group, the diagonal block per head,
     the chunk state per head, the off-diagonal term per head (skipped for a
     first chunk without initial state); of the short stage, the recurrence's
@@ -123,7 +126,8 @@ def work_model(w, short_len: int = 0) -> dict:
     # in calls of several sequences the chunk-state kernel finishes one-block
     # sequences (their slot traffic is its); state passing takes the others
     Qb = min(w.chunk_size, 128)
-    one_block = [not sh and w.batch > 1 and L <= Qb for L, sh in zip(lens, short)]
+    one_block = [not sh and (fused_walk or (w.batch > 1 and L <= Qb))
+                 for L, sh in zip(lens, short)]
     pool_r_one = sum(slot_b for b, o in enumerate(one_block) if o and hinit[b])
     pool_w_one = sum(slot_b for o in one_block if o)
     pool_r_long = sum(slot_b for b, sh in enumerate(short) if not sh and hinit[b]) - pool_r_one
@@ -279,7 +283,9 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     w = W.workload(args.workload)
-    model = work_model(w, pkg.ssd_scan_varlen_short_threshold(w.total_len, w.batch))
+    walk = pkg.ssd_scan_varlen_fused_walk(w.total_len, w.batch, w.nheads, w.head_dim,
+                                          w.ngroups, w.dstate, w.chunk_size)
+    model = work_model(w, pkg.ssd_scan_varlen_short_threshold(w.total_len, w.batch), walk)
     T = w.total_len
 
     def bf(a):
@@ -453,6 +459,8 @@ def run_ours(args, rank, world, local):
                    "head_dim": w.head_dim, "ngroups": w.ngroups, "dstate": w.dstate,
                    "chunk_size": w.chunk_size, "chunks": model["chunks"], "form": args.form,
                    "l2": f"flushed before every timed call ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "state_kernels": ("fused walk (chunk_state stage; state_passing empty)"
+                                     if walk else "chunk_state + state_passing"),
                    "parallelism": f"replicas x{world}"},
         "us_per_call": round(mean_ms_all * 1e3, 3),
         "us_per_call_median": round(statistics.median(times_ms) * 1e3, 3),
@@ -464,7 +472,8 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(tokens_all / (e2e_ms_all * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e2e_ms_all * 1e3, 3)},
-        "gpu_launches": K * pkg.ssd_scan_varlen_num_launches(T, w.batch),
+        "gpu_launches": K * pkg.ssd_scan_varlen_num_launches(T, w.batch, w.nheads, w.head_dim,
+                                                             w.ngroups, w.dstate, w.chunk_size),
         "clocks": clocks,
     }
     return result, w

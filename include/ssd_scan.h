@@ -247,11 +247,27 @@ SSD_API ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stre
 SSD_API const char *ssd_status_string(ssd_status_t status);
 
 /* Number of CUDA kernels one ssd_scan_varlen_fwd call launches for these sizes
- * (0 when batch == 0): chunk state and state passing, chunk scan when
- * total_len > 0, the short-sequence kernel when the call may hold short
- * sequences, and a block-map kernel for batches of more than 512 sequences.
- * Used to count launches when timing. */
-SSD_API int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch);
+ * (0 when batch == 0): chunk state and state passing (one fused kernel when
+ * ssd_scan_varlen_fused_walk says so), chunk scan when total_len > 0, the
+ * short-sequence kernel when the call may hold short sequences, and a
+ * block-map kernel for batches of more than 512 sequences.  Used to count
+ * launches when timing.  Reads the current device's SM count and L2 size. */
+SSD_API int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch, int32_t nheads,
+                                             int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                             int32_t chunk_size);
+
+/* 1 when a call with these sizes computes the chunk states and the
+ * inter-chunk state recurrence of the kernelindex page "Mamba chunk scan with
+ * segsum" in one persistent kernel that keeps the chunk states on chip (calls
+ * of long sequences -- 2048 tokens or more on average -- whose chunk states
+ * would exceed the L2 and whose (sequence, head group) items fill the GPU), 0
+ * when it writes them out and runs the recurrence as a kernel of its own.
+ * Both compute the same result up to rounding; this only says which kernels
+ * run.  0 for invalid sizes.  Reads the current device's SM count and L2
+ * size (152 SMs, 126 MB when no device answers). */
+SSD_API int32_t ssd_scan_varlen_fused_walk(int64_t total_len, int32_t batch, int32_t nheads,
+                                           int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                           int32_t chunk_size);
 
 /* The longest sequence (in tokens) that a call with these sizes gives to the
  * short-sequence kernel, the per-token recurrence of the Modular page

@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     ssd_scan_varlen_fwd_bf16_pool,
     ssd_scan_varlen_fwd_noalloc,
     ssd_scan_varlen_num_launches,
+    ssd_scan_varlen_fused_walk,
     ssd_scan_varlen_read_errors,
     ssd_scan_varlen_short_threshold,
     ssd_scan_varlen_workspace_size,

@@ -26,6 +26,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_read_errors",
     "ssd_status_string",
     "ssd_scan_varlen_num_launches",
+    "ssd_scan_varlen_fused_walk",
     "ssd_scan_varlen_short_threshold",
 )
 
@@ -83,7 +84,9 @@ def library() -> ctypes.CDLL:
     lib.ssd_status_string.restype = ctypes.c_char_p
     lib.ssd_status_string.argtypes = [ctypes.c_int]
     lib.ssd_scan_varlen_num_launches.restype = i32
-    lib.ssd_scan_varlen_num_launches.argtypes = [i64, i32]
+    lib.ssd_scan_varlen_num_launches.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+    lib.ssd_scan_varlen_fused_walk.restype = i32
+    lib.ssd_scan_varlen_fused_walk.argtypes = [i64, i32, i32, i32, i32, i32, i32]
     lib.ssd_scan_varlen_short_threshold.restype = i32
     lib.ssd_scan_varlen_short_threshold.argtypes = [i64, i32]
     _lib = lib
@@ -100,8 +103,19 @@ def ssd_scan_varlen_workspace_size(total_len: int, batch: int, nheads: int, head
                                                         ngroups, dstate, chunk_size))
 
 
-def ssd_scan_varlen_num_launches(total_len: int, batch: int) -> int:
-    return int(library().ssd_scan_varlen_num_launches(total_len, batch))
+def ssd_scan_varlen_num_launches(total_len: int, batch: int, nheads: int, head_dim: int,
+                                 ngroups: int, dstate: int, chunk_size: int) -> int:
+    return int(library().ssd_scan_varlen_num_launches(total_len, batch, nheads, head_dim,
+                                                      ngroups, dstate, chunk_size))
+
+
+def ssd_scan_varlen_fused_walk(total_len: int, batch: int, nheads: int, head_dim: int,
+                               ngroups: int, dstate: int, chunk_size: int) -> bool:
+    """True when a call of these sizes runs the fused chunk-state walk (one
+    kernel for the chunk states and the state recurrence) instead of the two
+    split kernels."""
+    return bool(library().ssd_scan_varlen_fused_walk(total_len, batch, nheads, head_dim,
+                                                     ngroups, dstate, chunk_size))
 
 
 def ssd_scan_varlen_short_threshold(total_len: int, batch: int) -> int:

@@ -1,6 +1,6 @@
 // C ABI of the scan (declared in include/ssd_scan.h): argument checks,
-// workspace carving, TMA descriptor encoding and the four stage launches on
-// the caller's stream.  No host synchronisation, no allocation.
+// workspace carving, TMA descriptor encoding and the stage launches on the
+// caller's stream.  No host synchronisation, no allocation.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -103,10 +103,12 @@ ssd_status_t check_sizes(int64_t T, int32_t batch, int32_t H, int32_t P, int32_t
         return SSD_ERR_UNSUPPORTED;
     const ssd::K1Config k1 = ssd::chunk_state_config(H, G, P, N);
     const ssd::K3Config k3 = ssd::chunk_scan_config(H, G, P, N);
+    const ssd::WalkConfig kw = ssd::state_walk_config(H, G, P, N, batch > 0 ? batch : 1, 1);
     if (k1.HB == 0 || k3.HB == 0)
         return SSD_ERR_UNSUPPORTED;
     if (k1.smem > static_cast<size_t>(ssd::kMaxSmemPerBlock) ||
-        k3.smem > static_cast<size_t>(ssd::kMaxSmemPerBlock))
+        k3.smem > static_cast<size_t>(ssd::kMaxSmemPerBlock) ||
+        kw.smem > static_cast<size_t>(ssd::kMaxSmemPerBlock))
         return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
 }
@@ -144,11 +146,28 @@ int32_t ssd_scan_varlen_short_threshold(int64_t total_len, int32_t batch)
     return batch > 0 ? short_len_of(total_len, batch) : 0;
 }
 
-int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch)
+int32_t ssd_scan_varlen_fused_walk(int64_t total_len, int32_t batch, int32_t nheads,
+                                   int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                   int32_t chunk_size)
+{
+    if (batch <= 0 ||
+        check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size) != SSD_OK)
+        return 0;
+    return ssd::use_state_walk(total_len, batch, nheads, ngroups, head_dim, dstate,
+                               ssd::block_tokens(chunk_size))
+               ? 1
+               : 0;
+}
+
+int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch, int32_t nheads,
+                                     int32_t head_dim, int32_t ngroups, int32_t dstate,
+                                     int32_t chunk_size)
 {
     if (batch <= 0)
         return 0;
-    return 2 + (total_len > 0 ? 1 : 0) + (short_path(total_len, batch) ? 1 : 0) +
+    const int walk = ssd_scan_varlen_fused_walk(total_len, batch, nheads, head_dim, ngroups,
+                                                dstate, chunk_size);
+    return (walk ? 1 : 2) + (total_len > 0 ? 1 : 0) + (short_path(total_len, batch) ? 1 : 0) +
            (batch > ssd::kMapBatchMax ? 1 : 0);
 }
 
@@ -238,7 +257,10 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.Q = Qb;
     p.dt_softplus = dt_softplus ? 1 : 0;
     p.short_len = short_len_of(total_len, batch);
-    p.finish_single = batch > 1 ? 1 : 0;
+    // calls of long sequences with many heads take the fused walk (the block
+    // states stay on chip); the others the split chunk-state / state-passing pair
+    const bool walk = ssd::use_state_walk(total_len, batch, nheads, ngroups, head_dim, dstate, Qb);
+    p.finish_single = (!walk && batch > 1) ? 1 : 0;
     p.max_chunks = static_cast<int32_t>(L.max_chunks);
     p.hdr = reinterpret_cast<ssd::WsHeader *>(ws + L.header);
     p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);
@@ -250,9 +272,11 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.sprev = reinterpret_cast<__nv_bfloat16 *>(ws + L.sprev);
 
     ssd::ChunkStateMaps m1;
+    ssd::StateWalkMaps mw;
     ssd::ChunkScanMaps m3;
     ssd::ShortScanMaps ms;
     std::memset(&m1, 0, sizeof m1);  // with total_len == 0 no kernel reads a map
+    std::memset(&mw, 0, sizeof mw);
     std::memset(&m3, 0, sizeof m3);
     std::memset(&ms, 0, sizeof ms);
     if (total_len > 0) {
@@ -266,6 +290,13 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                   make_map_3d(&m3.X, x, H * P, T, 1, xs, xs * T, 64, 1) &&
                   make_map_3d(&m3.Sprev, p.sprev, N, P, static_cast<uint64_t>(L.max_chunks) * H,
                               N * 2, P * N * 2, 64, 1);
+        if (ok && walk) {
+            // dt by TMA when its base and row pitch are 16-byte aligned
+            mw.B = m1.B;
+            mw.X = m1.X;
+            mw.dt_tma = aligned16(dt) && ts.dt % 8 == 0 &&
+                        make_map_plain(&mw.Dt, dt, H, T, 1, ts.dt * 2, ts.dt * 2 * T, 16, 64, 1);
+        }
         if (ok && p.short_len > 0) {
             const uint32_t R = static_cast<uint32_t>(ssd::short_scan_tile_rows(head_dim, dstate));
             ok = make_map_plain(&ms.X, x, H * P, T, 1, xs, xs * T, R, 8, 1) &&
@@ -283,12 +314,16 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                cudaEventRecord(static_cast<cudaEvent_t>(events[k]), stream) == cudaSuccess;
     };
     const bool pdl = events == nullptr;
-    // large batches: the block map first, the chunk-state kernel its dependent
+    // large batches: the block map first, the chunk-state kernel (or the walk)
+    // its dependent; with the walk the state-passing stage has no launch
     const bool mapped = p.table != nullptr;
-    if (!mark(0) || (mapped && ssd::launch_block_map(p, stream) != cudaSuccess) ||
-        ssd::launch_chunk_state(p, m1, stream, mapped && pdl) != cudaSuccess || !mark(1))
+    if (!mark(0) || (mapped && ssd::launch_block_map(p, stream) != cudaSuccess))
         return SSD_ERR_CUDA;
-    if (ssd::launch_state_passing(p, stream, pdl) != cudaSuccess || !mark(2))
+    if ((walk ? ssd::launch_state_walk(p, mw, stream, mapped && pdl)
+              : ssd::launch_chunk_state(p, m1, stream, mapped && pdl)) != cudaSuccess ||
+        !mark(1))
+        return SSD_ERR_CUDA;
+    if ((!walk && ssd::launch_state_passing(p, stream, pdl) != cudaSuccess) || !mark(2))
         return SSD_ERR_CUDA;
     if (total_len > 0 && ssd::launch_chunk_scan(p, m3, stream, pdl) != cudaSuccess)
         return SSD_ERR_CUDA;

@@ -66,51 +66,6 @@ __host__ __device__ inline K1Layout k1_layout(int NP, int n_mtiles, int HB)
     return L;
 }
 
-// The per-call bookkeeping, by one CTA of kThreads threads after its block
-// map (which wrote seq_first): the bad-slot checks, the two work lists of
-// sequence records (short ones for the short-sequence kernel, the others for
-// state passing) and the header (valid flag, block count).  `scratch` is the
-// block map's shared ints; 38 and 39 are used here.
-__device__ void call_bookkeeping(const ScanParams &p, const BlockInfo &bi, int32_t *scratch)
-{
-    const int tid = threadIdx.x;
-    if (p.pool != nullptr)
-        for (int b = tid; b < p.batch; b += kThreads)
-            if (static_cast<int64_t>(p.cache_idx[b]) >= p.max_slots)
-                record_error(p.hdr, kErrBadSlot);
-    int32_t *s_count = scratch + 38, *l_count = scratch + 39;   // past map_block's ints
-    if (tid == 0) {
-        *s_count = 0;
-        *l_count = 0;
-    }
-    __syncthreads();   // also orders map_block's seq_first writes before the reads
-    if (bi.valid)
-        for (int b = tid; b < p.batch; b += kThreads) {
-            SeqRec r;
-            r.t0 = p.qsl[b];
-            r.len = p.qsl[b + 1] - r.t0;
-            r.c_begin = p.seq_first[b];
-            r.c_end = p.seq_first[b + 1];
-            r.init = seq_init_index(p, b);
-            r.fin = seq_final_index(p, b);
-            // a sequence of one block may be finished by the chunk-state kernel
-            if (r.len <= p.short_len)
-                p.short_list[atomicAdd(s_count, 1)] = r;
-            else if (!p.finish_single || r.c_end - r.c_begin > 1)
-                p.long_list[atomicAdd(l_count, 1)] = r;
-        }
-    __syncthreads();
-    if (tid == 0) {
-        p.hdr->n_short = *s_count;
-        p.hdr->n_long = *l_count;
-        if (!bi.valid)
-            record_error(p.hdr, kErrBadQsl);
-        p.hdr->valid = bi.valid;
-        p.hdr->nchunks = bi.valid ? bi.total : 0;
-        __threadfence();
-    }
-}
-
 // Batches of more than kMapBatchMax sequences: one CTA maps every block once
 // into the block table (and does the bookkeeping); the block kernels, launched
 // as its programmatic dependents, look their block up instead of scanning
@@ -124,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) block_map_kernel(ScanParams p)
         p.hdr->errors = 0u;
     // a block index past every block: the scan only writes the tables
     const BlockInfo bi = map_block<kThreads>(p, int64_t(1) << 62, scratch, p.seq_first, p.table);
-    call_bookkeeping(p, bi, scratch);
+    call_bookkeeping<kThreads>(p, bi, scratch);
 }
 
 // kFinishSingle: a sequence's only block is finished here (batches of several
@@ -179,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
             p.hdr->errors = 0u;
         bi = map_block<kThreads>(p, blk, scratch, leader ? p.seq_first : nullptr);
         if (leader)
-            call_bookkeeping(p, bi, scratch);
+            call_bookkeeping<kThreads>(p, bi, scratch);
     }
     // the state-passing kernel may start launching; it waits for this grid
     // (with the block table, only once this CTA has read it, so that every

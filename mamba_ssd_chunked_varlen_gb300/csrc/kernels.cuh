@@ -28,6 +28,33 @@ K1Config chunk_state_config(int H, int G, int P, int N);
 cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
                                cudaStream_t stream, bool programmatic);
 
+// Stages 1, 2c and 3 fused (calls of long sequences with many heads): a
+// persistent walk over (sequence, head group, dstate tile) items that keeps
+// the block states on chip and writes the state entering every block (bf16)
+// and every sequence's final state.  Replaces chunk_state + state_passing for
+// the calls use_state_walk picks; with at most kMapBatchMax sequences its CTA
+// 0 also does the per-call bookkeeping.
+struct StateWalkMaps {
+    CUtensorMap B;   // bf16 (N, G, T), box {64, 1, 64}, 128-byte swizzle
+    CUtensorMap X;   // bf16 (H*P, T, 1), box {64, 64, 1}
+    CUtensorMap Dt;  // bf16 (H, T, 1), box {16, 64, 1}, no swizzle (when dt_tma)
+    int dt_tma;      // 1: dt rows are 16-byte aligned and go by TMA; 0: plain loads
+};
+struct WalkConfig {
+    int HB;       // heads per item (HB * head_dim <= 128, one B group)
+    int NP;       // HB * head_dim padded to 64 (64 or 128 columns)
+    int nT;       // 128-row dstate tiles
+    size_t smem;
+};
+WalkConfig state_walk_config(int H, int G, int P, int N, int batch, int sms);
+cudaError_t launch_state_walk(const ScanParams &p, const StateWalkMaps &maps, cudaStream_t stream,
+                              bool programmatic);
+// Whether a call takes the fused walk: every SM gets an item, the sequences
+// average at least 2048 tokens, and the block states the split design would
+// write and read back exceed the L2.  Uses the current device's SM count and
+// L2 size (152 SMs and 126 MB when no device answers).
+bool use_state_walk(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb);
+
 // Batches of more than kMapBatchMax sequences: one CTA scans query_start_loc
 // once, writes the block table and does the per-call bookkeeping; launched
 // before the chunk-state kernel, which then runs as its programmatic dependent.

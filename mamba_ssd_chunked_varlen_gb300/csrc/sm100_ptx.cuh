@@ -79,6 +79,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     return true;
 }
 
+// mbar_wait for threads that wait long and are not on the critical issue path:
+// between attempts the warp sleeps for about `sleep_ns`, leaving the issue
+// slots to the warps that work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t timeout_ns,
+                                                uint32_t sleep_ns)
+{
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        __nanosleep(sleep_ns);
+        if (globaltimer_ns() - t0 > timeout_ns)
+            return false;
+    }
+    return true;
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tensor-core operands written by threads).
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -236,6 +236,52 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
     return bi;
 }
 
+// The per-call bookkeeping, by one CTA of kThreads threads after its block
+// map (which wrote seq_first): the bad-slot checks, the two work lists of
+// sequence records (short ones for the short-sequence kernel, the others for
+// state passing or the fused walk) and the header (valid flag, block count).  `scratch` is the
+// block map's shared ints; 38 and 39 are used here.
+template <int kThreads>
+__device__ void call_bookkeeping(const ScanParams &p, const BlockInfo &bi, int32_t *scratch)
+{
+    const int tid = threadIdx.x;
+    if (p.pool != nullptr)
+        for (int b = tid; b < p.batch; b += kThreads)
+            if (static_cast<int64_t>(p.cache_idx[b]) >= p.max_slots)
+                record_error(p.hdr, kErrBadSlot);
+    int32_t *s_count = scratch + 38, *l_count = scratch + 39;   // past map_block's ints
+    if (tid == 0) {
+        *s_count = 0;
+        *l_count = 0;
+    }
+    __syncthreads();   // also orders map_block's seq_first writes before the reads
+    if (bi.valid)
+        for (int b = tid; b < p.batch; b += kThreads) {
+            SeqRec r;
+            r.t0 = p.qsl[b];
+            r.len = p.qsl[b + 1] - r.t0;
+            r.c_begin = p.seq_first[b];
+            r.c_end = p.seq_first[b + 1];
+            r.init = seq_init_index(p, b);
+            r.fin = seq_final_index(p, b);
+            // a sequence of one block may be finished by the chunk-state kernel
+            if (r.len <= p.short_len)
+                p.short_list[atomicAdd(s_count, 1)] = r;
+            else if (!p.finish_single || r.c_end - r.c_begin > 1)
+                p.long_list[atomicAdd(l_count, 1)] = r;
+        }
+    __syncthreads();
+    if (tid == 0) {
+        p.hdr->n_short = *s_count;
+        p.hdr->n_long = *l_count;
+        if (!bi.valid)
+            record_error(p.hdr, kErrBadQsl);
+        p.hdr->valid = bi.valid;
+        p.hdr->nchunks = bi.valid ? bi.total : 0;
+        __threadfence();
+    }
+}
+
 // Block `blk` from the block table (the block-map kernel's output; read only
 // after that kernel has completed).
 __device__ __forceinline__ BlockInfo lookup_block(const ScanParams &p, int64_t blk)

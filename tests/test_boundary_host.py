@@ -65,7 +65,8 @@ def test_workspace_size(lib):
 
 
 def test_launch_count(lib):
-    n = binding.ssd_scan_varlen_num_launches
+    def n(T, b, H=16, P=64, G=1, N=256, Q=256):
+        return binding.ssd_scan_varlen_num_launches(T, b, H, P, G, N, Q)
     assert n(4096, 1) == 3      # block states, state passing, output
     assert n(4096, 2) == 4      # + the short-sequence kernel (a batch may hold short ones)
     assert n(12, 1) == 4        # one sequence short enough for the per-token kernel
@@ -74,6 +75,21 @@ def test_launch_count(lib):
     assert n(10, 0) == 0
     assert n(5000, 512) == 4    # up to 512 sequences every CTA maps its own block
     assert n(5000, 513) == 5    # beyond, a block-map kernel writes a block table
+    # long sequences with many heads whose block states exceed the L2: block
+    # states and state passing in one fused kernel
+    assert n(32768, 4, 128, 64, 8, 128) == 3
+
+
+def test_fused_walk_choice(lib):
+    w = binding.ssd_scan_varlen_fused_walk
+    assert w(32768, 4, 128, 64, 8, 128, 256)           # 4 x 8192 tokens, 128 heads
+    assert w(12288, 3, 128, 64, 8, 128, 256)           # 3 x 4096 tokens
+    assert not w(4096, 1, 16, 64, 1, 256, 256)         # 32 items: too few for the GPU
+    assert not w(16384, 256, 64, 64, 1, 128, 256)      # short sequences
+    assert w(8192, 4, 128, 64, 8, 128, 256)            # 2048 tokens each, 268 MB of states
+    assert not w(16384, 8, 64, 32, 1, 64, 256)         # 2048 tokens each, 67 MB of states
+    assert not w(32768, 0, 128, 64, 8, 128, 256)
+    assert not w(32768, 4, 128, 64, 8, 512, 256)       # invalid sizes
 
 
 def test_short_threshold(lib):
@@ -86,7 +102,7 @@ def test_short_threshold(lib):
     # the launch count follows the threshold
     n = binding.ssd_scan_varlen_num_launches
     for T, b in [(4096, 1), (12, 1), (13, 1), (4096, 2), (0, 3)]:
-        assert n(T, b) == 2 + (T > 0) + (s(T, b) > 0)
+        assert n(T, b, 16, 64, 1, 256, 256) == 2 + (T > 0) + (s(T, b) > 0)
 
 
 def _call(lib, **over):

@@ -83,7 +83,8 @@ def test_large_batch_block_table():
     w = W.make_workload("big_batch", [int(v) for v in lens], 4, 32, 2, 32, 64,
                         max_slots=720, seed=72, has_init_p=0.6)
     import mamba_ssd_chunked_varlen_gb300 as pkg
-    assert pkg.ssd_scan_varlen_num_launches(w.total_len, w.batch) == 5
+    assert pkg.ssd_scan_varlen_num_launches(w.total_len, w.batch, w.nheads, w.head_dim, w.ngroups,
+                                            w.dstate, w.chunk_size) == 5
     y, pool, _, ws = run_cuda(w)
     assert pkg.ssd_scan_varlen_read_errors(ws) == 0
     y_ref, pool_ref = recurrence.run_workload(w)
