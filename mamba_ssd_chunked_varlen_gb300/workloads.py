@@ -162,11 +162,12 @@ def _ragged_lengths(rng: np.random.Generator, n: int, lo: int, hi: int, avoid_mu
 
 
 # Workload names, in the order they are listed for this op.
-WORKLOADS = ("tiny", "kernelindex", "ragged", "nemotron_h", "serving_mix", "decode")
+WORKLOADS = ("tiny", "kernelindex", "ragged", "nemotron_h", "serving_mix", "decode",
+             "nemotron_h_2k")
 
 
 def workload(name: str, seed: Optional[int] = None) -> Workload:
-    """The five standard workloads.
+    """The standard workloads.
 
     tiny          1 x 512 tokens, H=4, P=32, G=1, N=32, chunk 64, no initial state.
     kernelindex   1 x 4096 tokens, H=16, P=64, G=1, N=256, chunk 256: the head and
@@ -182,6 +183,9 @@ def workload(name: str, seed: Optional[int] = None) -> Workload:
     decode        256 sequences of 1 token each (a decode step of the serving
                   shape: H=64, P=64, G=1, N=128, chunk 256, 512-slot pool), every
                   sequence with an initial state: the pool read-modify-write case.
+    nemotron_h_2k nemotron_h with 4 x 2048 tokens: the smallest call of that
+                  shape whose chunk states exceed the L2 (so it takes the fused
+                  walk), ~1 GB on the device, for profiling the walk.
 
     For tiny and kernelindex the pool has 4 slots and one random slot is
     written, so that the untouched-slot check has something to check.
@@ -203,6 +207,9 @@ def workload(name: str, seed: Optional[int] = None) -> Workload:
         lens = np.random.default_rng([seed, 1]).geometric(1.0 / 64.0, 256)
         return make_workload(name, lens, 64, 64, 1, 128, 256, max_slots=512, seed=seed,
                              has_init_p=0.8)
+    if name == "nemotron_h_2k":
+        return make_workload(name, [2048] * 4, 128, 64, 8, 128, 256, max_slots=16,
+                             seed=seed, has_init_p=1.0)
     if name == "decode":
         return make_workload(name, [1] * 256, 64, 64, 1, 128, 256, max_slots=512, seed=seed,
                              has_init_p=1.0)
