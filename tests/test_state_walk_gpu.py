@@ -233,3 +233,69 @@ def test_walk_with_block_table():
             ref = pool_ref[s].astype(np.float64)
             rel = np.linalg.norm(pg[s] - ref) / np.linalg.norm(ref)
             assert rel <= STATE_REL_L2, f"sequence {b} slot {s}: {rel:.3e}"
+
+
+def test_walk_with_short_and_empty_sequences():
+    """A walk call may hold sequences short enough for the per-token kernel
+    (and empty ones): they are not walked, their slots are still written."""
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    w = W.make_workload("walk_mix", [4100, 0, 5, 4200, 4000], 128, 64, 8, 128, 256, max_slots=8,
+                        seed=408, has_init_p=0.6)
+    _assert_walk(w)
+    y, pool, _, ws = run_cuda(w)
+    assert pkg.ssd_scan_varlen_read_errors(ws) == 0
+    _check_sampled(w, y, pool, "walk with short sequences")
+
+
+def test_walk_bad_query_start_loc():
+    """A decreasing query_start_loc: the flag is set, nothing is written."""
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    w = _workload(seed=409)
+    _assert_walk(w)
+    d = to_device(w)
+    qsl = w.query_start_loc.copy()
+    qsl[1] = qsl[2] + 1                 # a negative length
+    d["query_start_loc"] = torch.from_numpy(qsl).cuda()
+    pool_before = d["ssm_pool"].clone()
+    y, pool, _, ws = run_cuda(w, dev=d)
+    flags = pkg.ssd_scan_varlen_read_errors(ws)
+    assert flags & pkg.binding.DEVERR_BAD_QUERY_START_LOC
+    assert not flags & pkg.binding.DEVERR_TIMEOUT
+    assert torch.equal(pool_before, pool)
+    assert torch.isnan(y.float()).all()
+
+
+def test_walk_bad_cache_index():
+    """A cache index past the pool: the flag is set, that sequence's slot
+    access is skipped (zero initial state, no write-back), the others are
+    computed as usual."""
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    w = _workload(seed=410)
+    _assert_walk(w)
+    w.cache_indices = np.array([w.cache_indices[0], 11, w.cache_indices[2]], np.uint32)
+    y, pool, _, ws = run_cuda(w)
+    flags = pkg.ssd_scan_varlen_read_errors(ws)
+    assert flags & pkg.binding.DEVERR_BAD_CACHE_INDEX
+    assert not flags & pkg.binding.DEVERR_TIMEOUT
+    pg = pool.cpu().numpy()
+    # the oracle with sequence 1 starting from zero and writing a spare slot
+    wr = copy.copy(w)
+    wr.ssm_pool = np.concatenate([w.ssm_pool, np.zeros_like(w.ssm_pool[:1])])
+    spare = w.ssm_pool.shape[0]
+    wr.cache_indices = np.array([w.cache_indices[0], spare, w.cache_indices[2]], np.uint32)
+    wr.has_initial_state = w.has_initial_state.copy()
+    wr.has_initial_state[1] = 0
+    yg = y_to_f64(y)
+    for heads in _head_ranges(w):
+        y_ref, pool_ref = recurrence.run_workload(wr, heads=heads)
+        check_y(yg[:, heads[0]:heads[1]], y_ref[:, heads[0]:heads[1]], what=f"bad slot {heads}")
+        for b in (0, 2):
+            s = int(w.cache_indices[b])
+            ref = pool_ref[s][heads[0]:heads[1]].astype(np.float64)
+            rel = np.linalg.norm(pg[s][heads[0]:heads[1]] - ref) / np.linalg.norm(ref)
+            assert rel <= STATE_REL_L2, f"bad slot: sequence {b} heads {heads}: {rel:.3e}"
+    written = {int(w.cache_indices[0]), int(w.cache_indices[2])}
+    for s in range(w.ssm_pool.shape[0]):
+        if s not in written:
+            assert np.array_equal(pg[s].view(np.uint32), w.ssm_pool[s].view(np.uint32)), \
+                f"slot {s} changed"
