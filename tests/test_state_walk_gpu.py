@@ -299,3 +299,21 @@ def test_walk_bad_cache_index():
         if s not in written:
             assert np.array_equal(pg[s].view(np.uint32), w.ssm_pool[s].view(np.uint32)), \
                 f"slot {s} changed"
+
+
+@pytest.mark.parametrize("variant", ["empty_optionals", "softplus_off"])
+def test_walk_optionals_and_softplus(variant):
+    """No D, no dt_bias and no has_initial_state (zero initial states), or dt
+    used as given (dt + dt_bias, no softplus)."""
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    if variant == "empty_optionals":
+        w = W.make_workload("walk_noopt", LENS, 128, 64, 8, 128, 256, max_slots=8, seed=411,
+                            with_D=False, with_dt_bias=False)
+        w.has_initial_state = None
+    else:
+        w = W.make_workload("walk_nosp", LENS, 128, 64, 8, 128, 256, max_slots=8, seed=412,
+                            has_init_p=0.7, dt_softplus=False)
+    _assert_walk(w)
+    y, pool, _, ws = run_cuda(w)
+    assert pkg.ssd_scan_varlen_read_errors(ws) == 0
+    _check_sampled(w, y, pool, f"walk {variant}")
