@@ -188,14 +188,40 @@ def stage_kernel(stage: str, walk: bool) -> str:
     return "state_walk" if walk and stage == "chunk_state" else stage
 
 
+def code_tokens(text: str) -> str:
+    """C++/CUDA source without comments and with whitespace runs collapsed, so
+    that a hash of it changes with the code only."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c == '"' or c == "'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(stage: str) -> str:
+    """Hash of the code (comments and layout ignored) of a kernel's source
+    file and the shared headers it includes."""
     path = os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc", f"{stage}.cu")
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba_ssd_chunked_varlen_gb300", "csrc")
     for p in (path, os.path.join(csrc, "sm100_ptx.cuh"), os.path.join(csrc, "ssd_common.cuh"),
               os.path.join(csrc, "ssd_device.cuh"), os.path.join(csrc, "kernels.cuh")):
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

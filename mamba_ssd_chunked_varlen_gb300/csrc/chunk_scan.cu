@@ -18,7 +18,8 @@
 // The heads form off-diagonal groups of up to two (their S_prev tiles stacked
 // along N of one MMA, C shared).  Warp roles (one CTA, 18 warps):
 //   warp 0    TMA producer: X of the CTA's heads, C and B; after the
-//             state-passing kernel, each group's S_prev tiles into B's space
+//             previous kernel (state passing, or the fused walk), each
+//             group's S_prev tiles into B's space
 //             (free once CB, then the previous group's Yoff, is done)
 //   warp 1    tcgen05 issuer: CB; group by group, Ydiag = Ldt X per head with
 //             the masked tile read from tensor memory, then the group's
@@ -29,8 +30,8 @@
 //             head's tile overlaps the MMA of the previous one); then the
 //             epilogue group by group, y staged through shared memory so that
 //             every warp store writes whole 128-byte rows
-// Everything before the S_prev loads is independent of the state-passing
-// kernel, so it overlaps that kernel (programmatic launch).
+// Everything before the S_prev loads is independent of the previous kernel,
+// so it may overlap that kernel's tail (programmatic launch).
 //
 // Tensor memory (512 columns): [0,128) CB, then the two masked-tile slots
 // (64 columns each, bf16 pairs); [128,384) Ydiag of up to four heads;
@@ -178,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // CTAs read it before letting later kernels launch)
     const BlockInfo bi = p.table != nullptr ? lookup_block(p, blk)
                                             : map_block<kThreads>(p, blk, scratch, nullptr);
-    // Every CTA waits for the state-passing grid before it leaves (those without
-    // an entering state would not otherwise), so that this grid completes only
+    // Every CTA waits for the previous grid before it leaves (those without an
+    // entering state would not otherwise), so that this grid completes only
     // after its predecessors and a dependent launch may rely on all of them.
     if (!bi.valid || bi.seq < 0) {
         pdl_wait();

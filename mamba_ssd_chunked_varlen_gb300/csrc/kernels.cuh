@@ -57,7 +57,8 @@ bool use_state_walk(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb
 
 // Batches of more than kMapBatchMax sequences: one CTA scans query_start_loc
 // once, writes the block table and does the per-call bookkeeping; launched
-// before the chunk-state kernel, which then runs as its programmatic dependent.
+// before the chunk-state kernel (or the fused walk), which then runs as its
+// programmatic dependent.
 cudaError_t launch_block_map(const ScanParams &p, cudaStream_t stream);
 
 // Stage 3: inter-block state passing; writes the state entering every block
@@ -68,7 +69,7 @@ cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool 
 // Short sequences (<= p.short_len <= kShortLenMax tokens, including empty
 // ones): the per-token recurrence on state tiles streamed through shared
 // memory, y and the final state written directly.  Launched after the
-// chunk-state kernel's checks.  Its cost grows with the tokens while the
+// bookkeeping's checks.  Its cost grows with the tokens while the
 // chunked kernels spend a whole 128-row block, and a block state written and
 // read back, on any sequence.  Measured on GB300 with batches of 256
 // sequences, the per-token path is the faster one up to 16 tokens with 64

@@ -33,8 +33,9 @@
 //   and frees a stage once its store has read it, with kStoreLag stores in
 //   flight so that it never waits on the one it just issued.
 //
-// The sequences come from the list the chunk-state kernel's bookkeeping CTA
-// wrote (one 32-byte record each); the chunked kernels give them no block.
+// The sequences come from the list the per-call bookkeeping CTA wrote (in the
+// chunk-state kernel, the fused walk or the block-map kernel; one 32-byte
+// record each); the chunked kernels give them no block.
 #include "kernels.cuh"
 #include "sm100_ptx.cuh"
 #include "ssd_device.cuh"
@@ -332,7 +333,7 @@ __global__ void __maxnreg__(96)
     }
     __syncthreads();
 
-    // the chunk-state kernel has checked query_start_loc and listed the short
+    // the bookkeeping has checked query_start_loc and listed the short
     // sequences; only then is anything read or written
     pdl_wait();
     if (!p.hdr->valid)
@@ -570,7 +571,7 @@ cudaError_t launch_short_scan(const ScanParams &p, const ShortScanMaps &maps, cu
         return e;
     cudaLaunchConfig_t cfg = {};
     // a persistent grid, one CTA per SM (fewer for small batches), over the
-    // tiles of the short sequences the chunk-state kernel listed
+    // tiles of the short sequences the bookkeeping listed
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -23,7 +23,7 @@ struct WsHeader {
     int32_t nchunks;   // blocks of the call
     int32_t valid;     // 1 when query_start_loc passed the device checks
     int32_t n_short;   // entries of the short-sequence work list
-    int32_t n_long;    // entries of the state-passing work list
+    int32_t n_long;    // entries of the long-sequence work list
     int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
@@ -45,8 +45,8 @@ struct alignas(16) BlockEntry {
     int32_t flags;   // 1: the sequence's first block, 2: its last
 };
 
-// One sequence of a work list, resolved by the chunk-state kernel's
-// bookkeeping CTA so that a consumer reaches all of it with one 32-byte read.
+// One sequence of a work list, resolved by the per-call bookkeeping CTA so
+// that a consumer reaches all of it with one 32-byte read.
 struct __align__(16) SeqRec {
     int32_t t0, len;          // its tokens
     int32_t c_begin, c_end;   // its blocks
@@ -141,7 +141,8 @@ struct ScanParams {
     WsHeader *hdr;
     int32_t *seq_first;   // (batch + 1): first block of each sequence, then the total
     SeqRec *short_list;   // the short sequences (hdr->n_short of them)
-    SeqRec *long_list;    // the other sequences (hdr->n_long), state passing's list
+    SeqRec *long_list;    // the other sequences (hdr->n_long): state passing's list, or
+                          // the fused walk's for batches above kMapBatchMax
     BlockEntry *table;    // per block, for batches above kMapBatchMax; else null (each
                           // CTA maps its own block)
     float *decay;         // [block][head] exp(sum of A*dt over the block)

@@ -239,8 +239,8 @@ __device__ BlockInfo map_block(const ScanParams &p, int64_t blk, int32_t *scratc
 // The per-call bookkeeping, by one CTA of kThreads threads after its block
 // map (which wrote seq_first): the bad-slot checks, the two work lists of
 // sequence records (short ones for the short-sequence kernel, the others for
-// state passing or the fused walk) and the header (valid flag, block count).  `scratch` is the
-// block map's shared ints; 38 and 39 are used here.
+// state passing or the fused walk) and the header (valid flag, block count).
+// `scratch` is the block map's shared ints; 38 and 39 are used here.
 template <int kThreads>
 __device__ void call_bookkeeping(const ScanParams &p, const BlockInfo &bi, int32_t *scratch)
 {

@@ -71,3 +71,18 @@ def test_single_process_reduce_is_identity():
     assert bench.dist_reduce(4.25, "max") == 4.25
     assert bench.dist_reduce(4.25, "sum") == 4.25
     bench.dist_barrier()   # no process group: a no-op
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The source hash that keys the committed ncu traffic tracks code, not
+    comments or layout."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = 'int f(int x) { // one\n  return x + 1; /* two\n lines */ }\nconst char *s = "// kept";\n'
+    b = 'int f(int x) {\n    return x + 1;\n}\nconst char *s = "// kept";  // note\n'
+    c = 'int f(int x) { return x + 2; }\nconst char *s = "// kept";\n'
+    assert bench.code_tokens(a) == bench.code_tokens(b)
+    assert bench.code_tokens(a) != bench.code_tokens(c)
+    assert '"// kept"' in bench.code_tokens(a)
+    h = bench.kernel_source_hash("chunk_scan")
+    assert len(h) == 16 and h == bench.kernel_source_hash("chunk_scan")
