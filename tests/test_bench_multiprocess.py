@@ -1,4 +1,5 @@
-"""The multi-process plumbing of bench.py on CPU (world size 2, gloo).
+"""bench.py's host logic on CPU: the multi-process plumbing (world size 2,
+gloo) and the source hash that keys the committed ncu traffic.
 
 The scan has no collective (one process per GPU runs an independent replica),
 so what bench.py adds for N > 1 is host logic: process-group setup from the
