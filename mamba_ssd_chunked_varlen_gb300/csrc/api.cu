@@ -167,8 +167,11 @@ int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch, int32_t n
         return 0;
     const int walk = ssd_scan_varlen_fused_walk(total_len, batch, nheads, head_dim, ngroups,
                                                 dstate, chunk_size);
+    const bool table =
+        ssd::use_block_table(total_len, batch, nheads, ngroups, head_dim, dstate,
+                             ssd::block_tokens(chunk_size), short_len_of(total_len, batch));
     return (walk ? 1 : 2) + (total_len > 0 ? 1 : 0) + (short_path(total_len, batch) ? 1 : 0) +
-           (batch > ssd::kMapBatchMax ? 1 : 0);
+           (table ? 1 : 0);
 }
 
 }  // extern "C"
@@ -266,7 +269,10 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);
     p.short_list = reinterpret_cast<ssd::SeqRec *>(ws + L.short_list);
     p.long_list = reinterpret_cast<ssd::SeqRec *>(ws + L.long_list);
-    p.table = batch > ssd::kMapBatchMax ? reinterpret_cast<ssd::BlockEntry *>(ws + L.table) : nullptr;
+    p.table = ssd::use_block_table(total_len, batch, nheads, ngroups, head_dim, dstate, Qb,
+                                   p.short_len)
+                  ? reinterpret_cast<ssd::BlockEntry *>(ws + L.table)
+                  : nullptr;
     p.decay = reinterpret_cast<float *>(ws + L.decay);
     p.schunk = reinterpret_cast<float *>(ws + L.schunk);
     p.sprev = reinterpret_cast<__nv_bfloat16 *>(ws + L.sprev);

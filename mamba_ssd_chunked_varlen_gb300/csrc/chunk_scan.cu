@@ -587,6 +587,22 @@ SmemOptIn s_smem_configured;
 
 }  // namespace
 
+bool use_block_table(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb, int short_len)
+{
+    if (batch > kMapBatchMax)
+        return true;
+    if (batch <= 0)
+        return false;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const K3Config c = chunk_scan_config(H, G, P, N);
+    if (c.HB == 0)
+        return false;
+    const int64_t ctas = max_chunks_bound(T, batch, Qb, short_len) * (H / c.HB);
+    return ctas > 2 * static_cast<int64_t>(sms);
+}
+
 K3Config chunk_scan_config(int H, int G, int P, int N)
 {
     K3Config c{};

@@ -55,6 +55,13 @@ cudaError_t launch_state_walk(const ScanParams &p, const StateWalkMaps &maps, cu
 // L2 size (152 SMs and 126 MB when no device answers).
 bool use_state_walk(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb);
 
+// Whether a call maps its blocks once in the block-map kernel: batches of more
+// than kMapBatchMax sequences, and calls whose chunk-scan grid would run more
+// than two waves of one CTA per SM (a per-CTA block map costs each wave a
+// query_start_loc round trip).  Uses the current device's SM count (152 when
+// no device answers).
+bool use_block_table(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb, int short_len);
+
 // Batches of more than kMapBatchMax sequences: one CTA scans query_start_loc
 // once, writes the block table and does the per-call bookkeeping; launched
 // before the chunk-state kernel (or the fused walk), which then runs as its

@@ -36,7 +36,8 @@ struct WsLayout {
 
 // Batches of more sequences than this map their blocks once, in a kernel of
 // their own that writes a block table, instead of in every CTA (a scan of
-// query_start_loc per CTA costs a round per 512 sequences).
+// query_start_loc per CTA costs a round per 512 sequences); so do calls whose
+// block kernels run in several waves (each wave would map again).
 constexpr int32_t kMapBatchMax = 512;
 
 // Where a block lies, as the block table records it.
@@ -94,7 +95,7 @@ __host__ __device__ inline WsLayout ws_layout(int64_t T, int32_t batch, int32_t 
     L.long_list = off;
     off = align256(off + sizeof(SeqRec) * static_cast<size_t>(batch));
     L.table = off;
-    off = align256(off + (batch > kMapBatchMax ? sizeof(BlockEntry) * mc : 0));
+    off = align256(off + sizeof(BlockEntry) * mc);
     L.decay = off;
     off = align256(off + sizeof(float) * mc * H);
     L.schunk = off;
@@ -143,7 +144,7 @@ struct ScanParams {
     SeqRec *short_list;   // the short sequences (hdr->n_short of them)
     SeqRec *long_list;    // the other sequences (hdr->n_long): state passing's list, or
                           // the fused walk's for batches above kMapBatchMax
-    BlockEntry *table;    // per block, for batches above kMapBatchMax; else null (each
+    BlockEntry *table;    // per block, when the block-map kernel runs; else null (each
                           // CTA maps its own block)
     float *decay;         // [block][head] exp(sum of A*dt over the block)
     float *schunk;        // [block][head][P][N] block states (zero initial state)

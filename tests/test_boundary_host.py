@@ -73,11 +73,16 @@ def test_launch_count(lib):
     assert n(13, 1) == 3
     assert n(0, 3) == 3         # empty sequences: no output kernel
     assert n(10, 0) == 0
-    assert n(5000, 512) == 4    # up to 512 sequences every CTA maps its own block
-    assert n(5000, 513) == 5    # beyond, a block-map kernel writes a block table
+    # a block-map kernel writes a block table for more than 512 sequences, or
+    # when the chunk-scan grid would run more than two waves (424 blocks x 4
+    # head groups here); otherwise every CTA maps its own block
+    assert n(5000, 512) == 5
+    assert n(5000, 513) == 5
+    assert n(5000, 30) == 4     # 70 blocks x 4 head groups: under two waves
     # long sequences with many heads whose block states exceed the L2: block
-    # states and state passing in one fused kernel
-    assert n(32768, 4, 128, 64, 8, 128) == 3
+    # states and state passing in one fused kernel (and, at 260 blocks x 32
+    # head groups, the block-map kernel)
+    assert n(32768, 4, 128, 64, 8, 128) == 4
 
 
 def test_fused_walk_choice(lib):

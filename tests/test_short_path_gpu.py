@@ -60,24 +60,21 @@ def test_short_sequence_alone_equals_in_batch():
         assert torch.equal(pool1[s].view(torch.int32), pool_all[s].view(torch.int32)), f"seq {b}: state"
 
 
-def _split_runs(w, cut):
-    """The workload as two calls: sequences [0, cut) and [cut, batch)."""
-    out = []
-    for lo, hi in ((0, cut), (cut, w.batch)):
-        t0, t1 = int(w.query_start_loc[lo]), int(w.query_start_loc[hi])
-        out.append(dataclasses.replace(
-            w, x=w.x[t0:t1], dt=w.dt[t0:t1], B=w.B[t0:t1], C=w.C[t0:t1],
-            query_start_loc=(w.query_start_loc[lo:hi + 1] - t0).astype(np.int32),
-            has_initial_state=w.has_initial_state[lo:hi],
-            cache_indices=w.cache_indices[lo:hi]))
-    return out
+def _sub_run(w, lo, hi, pool):
+    """Sequences [lo, hi) of `w` as a call of their own on `pool`."""
+    t0, t1 = int(w.query_start_loc[lo]), int(w.query_start_loc[hi])
+    return dataclasses.replace(
+        w, x=w.x[t0:t1], dt=w.dt[t0:t1], B=w.B[t0:t1], C=w.C[t0:t1],
+        query_start_loc=(w.query_start_loc[lo:hi + 1] - t0).astype(np.int32),
+        has_initial_state=w.has_initial_state[lo:hi], cache_indices=w.cache_indices[lo:hi],
+        ssm_pool=pool)
 
 
 def test_large_batch_block_table():
     """More than 512 sequences: a block-map kernel writes a block table that the
     block kernels read.  Every sequence must give the bits it gives in a call
-    of at most 512 sequences (where each CTA maps its own block), and the whole
-    must match the oracle."""
+    small enough for each CTA to map its own block (no block-map kernel), and
+    the whole must match the oracle."""
     rng = np.random.default_rng(71)
     lens = rng.choice([0, 1, 3, 7, 12, 13, 40, 128, 129, 300], size=700)
     w = W.make_workload("big_batch", [int(v) for v in lens], 4, 32, 2, 32, 64,
@@ -90,16 +87,18 @@ def test_large_batch_block_table():
     y_ref, pool_ref = recurrence.run_workload(w)
     check_y(y_to_f64(y), y_ref, what="700 sequences")
     check_slots(pool.cpu().numpy(), pool_ref, w.ssm_pool, w, what="700 sequences")
-    # the same sequences in two calls of 350
-    parts = _split_runs(w, 350)
-    w1 = parts[0]
-    y1, pool1, _, _ = run_cuda(w1)
-    w2 = dataclasses.replace(parts[1], ssm_pool=pool1.cpu().numpy())
-    y2, pool2, _, _ = run_cuda(w2)
-    t_cut = int(w.query_start_loc[350])
-    assert torch.equal(y[:t_cut].view(torch.int16), y1.view(torch.int16))
-    assert torch.equal(y[t_cut:].view(torch.int16), y2.view(torch.int16))
-    assert torch.equal(pool.view(torch.int32), pool2.view(torch.int32))
+    # the same sequences in calls of 35, each mapping its blocks per CTA
+    pool_k = w.ssm_pool
+    for lo in range(0, w.batch, 35):
+        hi = min(w.batch, lo + 35)
+        wk = _sub_run(w, lo, hi, pool_k)
+        assert pkg.ssd_scan_varlen_num_launches(wk.total_len, wk.batch, wk.nheads, wk.head_dim,
+                                                wk.ngroups, wk.dstate, wk.chunk_size) == 4
+        yk, poolk, _, _ = run_cuda(wk)
+        t0, t1 = int(w.query_start_loc[lo]), int(w.query_start_loc[hi])
+        assert torch.equal(y[t0:t1].view(torch.int16), yk.view(torch.int16)), f"sequences [{lo}, {hi})"
+        pool_k = poolk.cpu().numpy()
+    assert np.array_equal(pool.cpu().numpy().view(np.int32), pool_k.view(np.int32))
 
 
 def test_large_batch_bad_query_start_loc():
