@@ -318,3 +318,30 @@ def test_walk_optionals_and_softplus(variant):
     y, pool, _, ws = run_cuda(w)
     assert pkg.ssd_scan_varlen_read_errors(ws) == 0
     _check_sampled(w, y, pool, f"walk {variant}")
+
+
+# (heads, head_dim, groups, dstate, chunk, lengths, options): sizes that take
+# the walk with every instantiation and tile count: 128 or 64 columns per item,
+# one to eight heads per item, one or two dstate tiles (144: a mostly empty
+# second tile), 64- to 256-token chunks, 1 to 16 groups, a short sequence
+# beside the long ones, empty optionals and softplus off
+WALK_SHAPES = [
+    (64, 128, 4, 128, 128, [4100, 5003, 3900, 4500], {}),
+    (96, 32, 3, 256, 256, [2500, 3000, 2100, 2900, 2600], {}),
+    (256, 16, 16, 144, 64, [2050, 2600, 3100], {}),
+    (128, 64, 1, 64, 256, [6000, 7000], {"with_D": False}),
+    (80, 64, 5, 256, 128, [3000, 4000, 2500, 7], {}),
+    (128, 64, 8, 128, 256, [3000, 3500, 2900, 2700], {"dt_softplus": False, "with_dt_bias": False}),
+]
+
+
+@pytest.mark.parametrize("case", range(len(WALK_SHAPES)))
+def test_walk_shapes(case):
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    H, P, G, N, Q, lens, opts = WALK_SHAPES[case]
+    w = W.make_workload(f"walk_shape{case}", lens, H, P, G, N, Q, max_slots=len(lens) + 3,
+                        seed=420 + case, has_init_p=0.6, **opts)
+    _assert_walk(w)
+    y, pool, _, ws = run_cuda(w)
+    assert pkg.ssd_scan_varlen_read_errors(ws) == 0
+    _check_sampled(w, y, pool, f"walk shape {case}")
