@@ -77,10 +77,11 @@ cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool 
 // ones): the per-token recurrence on state tiles streamed through shared
 // memory, y and the final state written directly.  Launched after the
 // bookkeeping's checks.  Its cost grows with the tokens while the
-// chunked kernels spend a whole 128-row block, and a block state written and
-// read back, on any sequence.  Measured on GB300 with batches of 256
-// sequences, the per-token path is the faster one up to 16 tokens with 64
-// heads of 64 x 128, up to about 14 with 32 heads of 64 x 256: 12 holds both.
+// chunked kernels spend a whole 128-row block on any sequence.  Measured on
+// GB300 with batches of 256 sequences of L tokens, 64 heads of 64 x 128, each
+// with an initial state: per-token path 598 us at L = 12, 692 us at 13; the
+// chunked path 669-672 us for L = 13..20.  The crossover lies between 12 and
+// 13.
 constexpr int kShortLenMax = 12;
 struct ShortScanMaps {
     CUtensorMap X;  // bf16 (H*P, T, 1), box {tile rows, 8, 1}, no swizzle
