@@ -15,9 +15,10 @@ Prints ONE JSON line on rank 0:
   value       tokens/s over all ranks (replicas: every rank runs the same
               independent workload; weak scaling), from CUDA events around
               each call on the launching stream
-  e2e         the same metric through the public API with host buffers: the
-              pinned-host -> device copies of the step's inputs, the call and
-              the device -> host copy of y inside the timed region
+  e2e         the same metric through the public API with host buffers
+              (ssd_scan_varlen_fwd_host: the pinned-host -> device copies of
+              the step's inputs, the scan and the device -> host copy of y,
+              overlapped piece by piece, all inside the timed region)
   roofline    the dominant kernel's achieved bytes (or flops) per launch over
               its event-timed duration, against the measured peak
   cpu_baseline  the fp64 oracle on this machine's host cores (a bounded sample)
@@ -441,20 +442,39 @@ def run_ours(args, rank, world, local):
     d2h = y_host.numel() * 2
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(Ke)]
+    # the in-place form goes through the host-buffer entry point (its copies
+    # in, the scan and y's copy out overlap piece by piece); the other forms
+    # copy the inputs, call the device entry point and copy y back
+    host_call = args.form == "inplace"
+    if host_call:
+        hb = {k: host[k].view(torch.bfloat16) for k in ("x", "dt", "B", "C")}
+        y_hb = y_host.view(torch.bfloat16)
+        hws = pkg.alloc_host_workspace(host["qsl"], w.nheads, w.head_dim, w.ngroups, w.dstate,
+                                       w.chunk_size, args.e2e_pieces, device=dev)
+        e2e_pieces = len(pkg.ssd_scan_varlen_host_plan(
+            host["qsl"], w.nheads, w.head_dim, w.ngroups, w.dstate, w.chunk_size,
+            args.e2e_pieces)) + 1
     for k in range(Ke):
         flush.fill_(k)
         eev[k][0].record(stream)
-        for key, hv in host.items():
-            dev_in[key].copy_(hv, non_blocking=True)
-        dd = {key: (dev_in[key].view(torch.bfloat16) if key in ("x", "dt", "B", "C") else
-                    dev_in[key]) for key in dev_in}
-        call(dd=dd)
-        y_host.copy_(y.view(torch.int16), non_blocking=True)
+        if host_call:
+            pkg.ssd_scan_varlen_fwd_host(
+                y_hb, hb["x"], hb["dt"], d["A"], hb["B"], hb["C"], d["D"], d["dt_bias"],
+                d["pool"], host["qsl"], host["hinit"], host["cidx"], chunk_size=w.chunk_size,
+                dt_softplus=w.dt_softplus, pieces=args.e2e_pieces, workspace=hws, stream=stream)
+        else:
+            for key, hv in host.items():
+                dev_in[key].copy_(hv, non_blocking=True)
+            dd = {key: (dev_in[key].view(torch.bfloat16) if key in ("x", "dt", "B", "C") else
+                        dev_in[key]) for key in dev_in}
+            call(dd=dd)
+            y_host.copy_(y.view(torch.int16), non_blocking=True)
         eev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / Ke
     e2e_ms_all = dist_reduce(e2e_ms, "max")
-    flags = pkg.ssd_scan_varlen_read_errors(ws, stream)
+    flags = (pkg.ssd_scan_varlen_host_read_errors(hws, stream) if host_call else 0) | \
+        pkg.ssd_scan_varlen_read_errors(ws, stream)
     if flags:
         raise RuntimeError(f"device error flags {flags:#x}")
 
@@ -503,7 +523,9 @@ def run_ours(args, rank, world, local):
         "stages_us": {s: round(stage_ms[s] * 1e3, 3) for s in STAGES},
         "e2e": {"value": round(tokens_all / (e2e_ms_all * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "us_per_step": round(e2e_ms_all * 1e3, 3)},
+                "us_per_step": round(e2e_ms_all * 1e3, 3),
+                "api": "ssd_scan_varlen_fwd_host" if host_call else "copies + device entry point",
+                "pieces": e2e_pieces if host_call else 1},
         "gpu_launches": K * pkg.ssd_scan_varlen_num_launches(T, w.batch, w.nheads, w.head_dim,
                                                              w.ngroups, w.dstate, w.chunk_size),
         "clocks": clocks,
@@ -596,6 +618,8 @@ def main(argv=None):
                          "fused projection buffer (the e2e leg copies contiguous inputs); "
                          "bf16pool: ssd_scan_varlen_fwd_bf16_pool (bf16 slot pool); "
                          "the per-stage attribution always uses the in-place profiled call")
+    ap.add_argument("--e2e-pieces", type=int, default=0,
+                    help="pieces of the host-buffer call in the e2e leg (0: its own choice)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -24,9 +24,11 @@
  *
  * Conventions for every entry point:
  *   - all tensor pointers are DEVICE pointers to contiguous row-major data
- *     with the shapes listed at ssd_scan_varlen_fwd; the caller owns them;
- *   - calls are asynchronous on `stream`; no entry point except
- *     ssd_scan_varlen_read_errors synchronizes;
+ *     with the shapes listed at ssd_scan_varlen_fwd (ssd_scan_varlen_fwd_host
+ *     takes its per-step tensors in host memory, as documented there); the
+ *     caller owns them;
+ *   - calls are asynchronous on `stream`; no entry point except the two
+ *     read_errors functions synchronizes;
  *   - a status other than SSD_OK from a host-side check means that nothing
  *     was launched and no memory was written.
  */
@@ -242,6 +244,89 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd_noalloc(
  * any flag is set, SSD_OK otherwise. */
 SSD_API ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stream_t stream,
                                          uint32_t *flags);
+
+/* ---- End-to-end call with host buffers --------------------------------
+ *
+ * The pages have no counterpart to this entry point.  It is for a caller
+ * whose per-step tensors live in host memory: it copies them in, runs the
+ * scan and copies y back, and overlaps the three.  The token range is cut
+ * into up to SSD_HOST_MAX_PIECES pieces.  Piece k's inputs are copied on one
+ * internal stream, its scan runs on `stream` once they have landed, and its
+ * y is copied back on a second internal stream while later pieces are still
+ * copied in or computed.
+ *
+ * Cuts fall on a sequence boundary or inside a sequence at a multiple of the
+ * block length (min(chunk_size, 128) tokens) from its start, so every block
+ * is the one the single call would form.  A sequence cut in two runs as two
+ * parts: the first writes its running state to the sequence's slot, and the
+ * second starts from that slot (as a continuation with an initial state).
+ * The running state is fp32 in both cases, so the result matches one
+ * ssd_scan_varlen_fwd call within the parity bounds.  The pieces' kernels
+ * run one after another on `stream`.
+ *
+ * Arguments as ssd_scan_varlen_fwd, except:
+ *   y_host, x_host, dt_host, B_host, C_host   host memory, same shapes and types;
+ *                          pinned (page-locked) memory is needed for the overlap
+ *                          (pageable memory works, but its copies do not overlap)
+ *   query_start_loc_host, has_initial_state_host (or NULL), cache_indices_host
+ *                          host arrays; checked on the host (qsl from 0, never
+ *                          decreasing, ending at total_len; slots < max_slots):
+ *                          SSD_ERR_INVALID_ARG without launching otherwise
+ *   A, D, dt_bias, ssm_pool   device memory, as for ssd_scan_varlen_fwd
+ *   pieces                 number of pieces asked for (0: one per ~6 MiB of
+ *                          x, dt, B and C, 1 to SSD_HOST_MAX_PIECES); fewer
+ *                          are used when cuts coincide
+ *   workspace              device scratch of at least
+ *                          ssd_scan_varlen_host_workspace_size bytes (256-byte
+ *                          aligned).  It holds the device copies of the
+ *                          inputs and of y and one scan workspace per piece.
+ *
+ * Host memory must stay valid until `stream` has passed the call (y_host is
+ * written by then).  All work is ordered after earlier work on `stream`, and
+ * later work on `stream` is ordered after all of it.  The two internal copy
+ * streams of each device are created on the first call and are shared by
+ * all calls on that device, so calls from several streams serialise their
+ * copies.  The pieces' small arrays (local query_start_loc, slots, flags)
+ * are written at call time into one of four pinned host buffers per device
+ * that the library keeps (grown as needed, held until the process exits);
+ * a call waits on the host only if that buffer's copy from four calls
+ * earlier has not run yet.  So the call cannot be captured into a CUDA
+ * graph.  Device-side error flags are read with
+ * ssd_scan_varlen_host_read_errors. */
+#define SSD_HOST_MAX_PIECES 8
+
+/* Bytes of workspace ssd_scan_varlen_fwd_host needs for this call (0 when
+ * the sizes are unsupported or query_start_loc_host is invalid). */
+SSD_API size_t ssd_scan_varlen_host_workspace_size(const int32_t *query_start_loc_host,
+                                                   int64_t total_len, int32_t batch,
+                                                   int32_t nheads, int32_t head_dim,
+                                                   int32_t ngroups, int32_t dstate,
+                                                   int32_t chunk_size, int32_t pieces);
+
+/* The token positions where ssd_scan_varlen_fwd_host cuts this call: writes
+ * the cuts (strictly increasing, inside (0, total_len)) to cuts_out, at most
+ * SSD_HOST_MAX_PIECES - 1 of them, and returns the number of pieces (cuts +
+ * 1), or -1 when query_start_loc_host is invalid or chunk_size unsupported.
+ * Host only: no device call. */
+SSD_API int32_t ssd_scan_varlen_host_plan(const int32_t *query_start_loc_host, int64_t total_len,
+                                          int32_t batch, int32_t nheads, int32_t head_dim,
+                                          int32_t ngroups, int32_t dstate, int32_t chunk_size,
+                                          int32_t pieces, int64_t *cuts_out);
+
+SSD_API ssd_status_t ssd_scan_varlen_fwd_host(
+    void *y_host, const void *x_host, const void *dt_host, const float *A, const void *B_host,
+    const void *C_host, const float *D, const float *dt_bias, float *ssm_pool,
+    const int32_t *query_start_loc_host, const uint8_t *has_initial_state_host,
+    const uint32_t *cache_indices_host, int64_t total_len, int32_t batch, int32_t nheads,
+    int32_t head_dim, int32_t ngroups, int32_t dstate, int64_t max_slots, int32_t chunk_size,
+    int32_t dt_softplus, int32_t pieces, void *workspace, size_t workspace_bytes,
+    ssd_stream_t stream);
+
+/* Synchronizes `stream` and returns the OR of the device-side error flags
+ * (SSD_DEVERR_*) of every piece of the last ssd_scan_varlen_fwd_host call
+ * that used `workspace`.  Returns SSD_ERR_DEVICE if any flag is set. */
+SSD_API ssd_status_t ssd_scan_varlen_host_read_errors(const void *workspace, ssd_stream_t stream,
+                                                      uint32_t *flags);
 
 /* A static string naming a status code. */
 SSD_API const char *ssd_status_string(ssd_status_t status);

@@ -7,6 +7,7 @@ include/ssd_scan.h); ``binding`` is its thin Python front end and
 from .binding import (  # noqa: F401
     EXPORTED_SYMBOLS,
     SSDError,
+    alloc_host_workspace,
     alloc_workspace,
     library,
     ssd_scan_varlen_fwd,
@@ -15,6 +16,10 @@ from .binding import (  # noqa: F401
     ssd_scan_varlen_fwd_strided,
     ssd_scan_varlen_fwd_bf16_pool,
     ssd_scan_varlen_fwd_noalloc,
+    ssd_scan_varlen_fwd_host,
+    ssd_scan_varlen_host_plan,
+    ssd_scan_varlen_host_read_errors,
+    ssd_scan_varlen_host_workspace_size,
     ssd_scan_varlen_num_launches,
     ssd_scan_varlen_fused_walk,
     ssd_scan_varlen_read_errors,

@@ -28,7 +28,13 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_num_launches",
     "ssd_scan_varlen_fused_walk",
     "ssd_scan_varlen_short_threshold",
+    "ssd_scan_varlen_host_workspace_size",
+    "ssd_scan_varlen_host_plan",
+    "ssd_scan_varlen_fwd_host",
+    "ssd_scan_varlen_host_read_errors",
 )
+
+HOST_MAX_PIECES = 8  # SSD_HOST_MAX_PIECES
 
 SSD_OK = 0
 SSD_ERR_TOO_LARGE = 6
@@ -89,6 +95,16 @@ def library() -> ctypes.CDLL:
     lib.ssd_scan_varlen_fused_walk.argtypes = [i64, i32, i32, i32, i32, i32, i32]
     lib.ssd_scan_varlen_short_threshold.restype = i32
     lib.ssd_scan_varlen_short_threshold.argtypes = [i64, i32]
+    lib.ssd_scan_varlen_host_workspace_size.restype = sz
+    lib.ssd_scan_varlen_host_workspace_size.argtypes = [vp, i64, i32, i32, i32, i32, i32, i32, i32]
+    lib.ssd_scan_varlen_host_plan.restype = i32
+    lib.ssd_scan_varlen_host_plan.argtypes = [vp, i64, i32, i32, i32, i32, i32, i32, i32,
+                                              ctypes.POINTER(ctypes.c_int64)]
+    lib.ssd_scan_varlen_fwd_host.restype = ctypes.c_int
+    lib.ssd_scan_varlen_fwd_host.argtypes = ([vp] * 12 + [i64, i32, i32, i32, i32, i32, i64, i32,
+                                                          i32, i32] + [vp, sz, vp])
+    lib.ssd_scan_varlen_host_read_errors.restype = ctypes.c_int
+    lib.ssd_scan_varlen_host_read_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     _lib = lib
     return lib
 
@@ -339,3 +355,111 @@ def alloc_workspace(total_len: int, batch: int, nheads: int, head_dim: int, ngro
     if n == 0:
         raise SSDError(2, "ssd_scan_varlen_workspace_size")
     return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+# ---- end-to-end call with host buffers
+
+def _hptr(t, what: str, dtype=None, allow_none: bool = False):
+    """Pointer to a contiguous CPU tensor (pinned for overlapped copies)."""
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{what} is required")
+    if t.is_cuda:
+        raise ValueError(f"{what} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} must have dtype {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr() or 0)
+
+
+def _host_qsl(query_start_loc_host):
+    import torch
+    if query_start_loc_host.is_cuda or query_start_loc_host.dtype != torch.int32:
+        raise ValueError("query_start_loc_host must be an int32 CPU tensor")
+    return query_start_loc_host.contiguous()
+
+
+def ssd_scan_varlen_host_plan(query_start_loc_host, nheads: int, head_dim: int, ngroups: int,
+                              dstate: int, chunk_size: int, pieces: int = 0):
+    """Token positions where ssd_scan_varlen_fwd_host cuts a call (a list of
+    cuts; pieces = len + 1).  Host only."""
+    q = _host_qsl(query_start_loc_host)
+    batch = q.numel() - 1
+    total = int(q[-1]) if batch >= 0 else 0
+    out = (ctypes.c_int64 * HOST_MAX_PIECES)()
+    n = library().ssd_scan_varlen_host_plan(ctypes.c_void_p(q.data_ptr()), total, batch,
+                                            nheads, head_dim, ngroups, dstate,
+                                            int(chunk_size), int(pieces), out)
+    if n < 0:
+        raise SSDError(1, "ssd_scan_varlen_host_plan")
+    return [int(out[i]) for i in range(n - 1)]
+
+
+def ssd_scan_varlen_host_workspace_size(query_start_loc_host, nheads: int, head_dim: int,
+                                        ngroups: int, dstate: int, chunk_size: int,
+                                        pieces: int = 0) -> int:
+    q = _host_qsl(query_start_loc_host)
+    batch = q.numel() - 1
+    return int(library().ssd_scan_varlen_host_workspace_size(
+        ctypes.c_void_p(q.data_ptr()), int(q[-1]), batch, nheads, head_dim, ngroups, dstate,
+        int(chunk_size), int(pieces)))
+
+
+def alloc_host_workspace(query_start_loc_host, nheads: int, head_dim: int, ngroups: int,
+                         dstate: int, chunk_size: int, pieces: int = 0, device="cuda"):
+    import torch
+    n = ssd_scan_varlen_host_workspace_size(query_start_loc_host, nheads, head_dim, ngroups,
+                                            dstate, chunk_size, pieces)
+    if n == 0:
+        raise SSDError(2, "ssd_scan_varlen_host_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def ssd_scan_varlen_fwd_host(y_host, x_host, dt_host, A, B_host, C_host, D, dt_bias, ssm_pool,
+                             query_start_loc_host, has_initial_state_host, cache_indices_host,
+                             *, chunk_size: int, dt_softplus: bool = True, pieces: int = 0,
+                             workspace=None, stream=None) -> None:
+    """The scan with y, x, dt, B, C and the int arrays in host memory (CPU
+    tensors; pin them for overlapped copies) and A, D, dt_bias, ssm_pool on
+    the device.  The inputs are copied in, scanned and y copied back in
+    pieces that overlap; y_host is written once `stream` has passed the call.
+    workspace: a uint8 CUDA tensor of ssd_scan_varlen_host_workspace_size
+    bytes."""
+    import torch
+    if workspace is None:
+        raise ValueError("workspace is required (see ssd_scan_varlen_host_workspace_size)")
+    T, H, P = x_host.shape
+    G, N = B_host.shape[1], B_host.shape[2]
+    q = _host_qsl(query_start_loc_host)
+    batch = q.numel() - 1
+    if has_initial_state_host is not None and has_initial_state_host.dtype == torch.bool:
+        has_initial_state_host = has_initial_state_host.view(torch.uint8)
+    if cache_indices_host.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("cache_indices_host must be int32 or uint32")
+    st = library().ssd_scan_varlen_fwd_host(
+        _hptr(y_host, "y_host", torch.bfloat16), _hptr(x_host, "x_host", torch.bfloat16),
+        _hptr(dt_host, "dt_host", torch.bfloat16), _ptr(A, "A", torch.float32),
+        _hptr(B_host, "B_host", torch.bfloat16), _hptr(C_host, "C_host", torch.bfloat16),
+        _ptr(D, "D", torch.float32, True), _ptr(dt_bias, "dt_bias", torch.float32, True),
+        _ptr(ssm_pool, "ssm_pool", torch.float32), ctypes.c_void_p(q.data_ptr()),
+        _hptr(has_initial_state_host, "has_initial_state_host", torch.uint8, True),
+        _hptr(cache_indices_host, "cache_indices_host"),
+        T, batch, H, P, G, N, ssm_pool.shape[0], int(chunk_size), int(bool(dt_softplus)),
+        int(pieces), _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan_varlen_fwd_host")
+
+
+def ssd_scan_varlen_host_read_errors(workspace, stream=None) -> int:
+    """Synchronize the stream and return the OR of the device-side error flags
+    of the last ssd_scan_varlen_fwd_host call that used this workspace."""
+    import torch
+    flags = ctypes.c_uint32(0)
+    st = library().ssd_scan_varlen_host_read_errors(_ptr(workspace, "workspace", torch.uint8),
+                                                    _stream_handle(stream), ctypes.byref(flags))
+    if st not in (SSD_OK, 5):
+        raise SSDError(st, "ssd_scan_varlen_host_read_errors")
+    return int(flags.value)

@@ -163,3 +163,61 @@ def test_states_form_host_checks(lib):
     assert _call_states(lib, N=512) == 2
     assert _call_states(lib, ws=None) == 3
     assert _call_states(lib, batch=0, final=None) == 0  # empty batch: nothing to do
+
+
+def _qsl(lens):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+
+
+def test_host_call_plan(lib):
+    """Cuts of the host-buffer call: inside (0, T), increasing, each on a
+    sequence boundary or a block boundary of the sequence it falls in, at
+    most the pieces asked for (0: one per 6 MiB of x, dt, B and C, 1 to 8)."""
+    def plan(q, Q, n, shape=(16, 64, 1, 256)):
+        return binding.ssd_scan_varlen_host_plan(q, *shape, Q, n)
+    one = _qsl([4096])
+    assert plan(one, 256, 1) == []
+    assert plan(one, 256, 2) == [2048]
+    assert plan(one, 256, 3) == [1408, 2688]          # 1365 and 2730 to the nearest 128
+    assert plan(one, 256, 0) == [2048]                # 12.7 MB of inputs
+    # 36.2 MB: 5 pieces, targets 819, 1638, 2457, 3276 to the nearest 128
+    assert plan(one, 256, 0, (64, 64, 1, 128)) == [768, 1664, 2432, 3328]
+    assert plan(_qsl([1000]), 256, 0) == []
+    assert plan(one, 256, 100) == [512 * k for k in range(1, 8)]   # capped at 8 pieces
+    assert plan(one, 64, 3) == [1344, 2752]           # 64-token blocks
+    import numpy as np
+    lens = [700, 136, 0, 900, 12, 600, 0]
+    q = _qsl(lens)
+    qs = q.tolist()
+    for Q in (64, 128, 256):
+        Qb = min(Q, 128)
+        for n in range(1, 9):
+            cuts = plan(q, Q, n)
+            assert len(cuts) <= n - 1
+            assert all(0 < c < int(q[-1]) for c in cuts)
+            assert all(a < b for a, b in zip(cuts, cuts[1:]))
+            for c in cuts:
+                # on a sequence boundary, or a block edge of the sequence holding c
+                b = int(np.searchsorted(qs, c, side="right")) - 1
+                assert c in qs or (c - qs[b]) % Qb == 0, (Q, n, c)
+    # 1550 falls in the second sequence: 100 + 11 blocks
+    assert plan(_qsl([100, 3000]), 128, 2) == [1508]
+    # 1690 rounds to 1728, past the end of its sequence: the cut is that end
+    assert plan(_qsl([1600, 100, 1680]), 128, 2) == [1700]
+
+
+def test_host_call_checks(lib):
+    """Invalid host query_start_loc: no plan, no workspace size."""
+    import torch
+    bad = torch.tensor([0, 300, 200], dtype=torch.int32)
+    with pytest.raises(binding.SSDError):
+        binding.ssd_scan_varlen_host_plan(bad, 4, 32, 2, 64, 128, 2)
+    assert binding.ssd_scan_varlen_host_workspace_size(bad, 4, 32, 2, 64, 128, 2) == 0
+    ok = torch.tensor([0, 300, 500], dtype=torch.int32)
+    n = binding.ssd_scan_varlen_host_workspace_size(ok, 4, 32, 2, 64, 128, 2)
+    # the device copies of x, dt, B, C and y plus one scan workspace per piece
+    assert n >= 500 * (2 * 4 * 32 * 2 + 4 * 2 + 2 * 2 * 64 * 2) + \
+        binding.ssd_scan_varlen_workspace_size(500, 2, 4, 32, 2, 64, 128)
+    assert binding.ssd_scan_varlen_host_workspace_size(ok, 4, 32, 2, 48 * 8, 128, 2) == 0
