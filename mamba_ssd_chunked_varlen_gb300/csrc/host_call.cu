@@ -352,6 +352,15 @@ ssd_status_t ssd_scan_varlen_fwd_host(
         !ok(cudaEventRecord(ds->stage_done[slot], ds->h2d)))
         return SSD_ERR_CUDA;
     ds->stage_used[slot] = true;
+    // after a failure past this point, later work on `stream` still waits
+    // for every copy already queued on the internal streams
+    auto fail = [&](ssd_status_t st) {
+        if (cudaEventRecord(ds->in_done[0], ds->h2d) == cudaSuccess)
+            (void)cudaStreamWaitEvent(stream, ds->in_done[0], 0);
+        if (cudaEventRecord(ds->end, ds->d2h) == cudaSuccess)
+            (void)cudaStreamWaitEvent(stream, ds->end, 0);
+        return st;
+    };
 
     // inputs, piece by piece, on the copy-in stream
     for (int k = 0; k < np; ++k) {
@@ -366,9 +375,9 @@ ssd_status_t ssd_scan_varlen_fwd_host(
                                  cudaMemcpyHostToDevice, ds->h2d)) ||
              !ok(cudaMemcpyAsync(ws + pl.C_off + a * rb, hC + a * rb, n * rb,
                                  cudaMemcpyHostToDevice, ds->h2d))))
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
         if (!ok(cudaEventRecord(ds->in_done[k], ds->h2d)))
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
     }
 
     // each piece's scan on the caller's stream once its inputs landed, and
@@ -381,7 +390,7 @@ ssd_status_t ssd_scan_varlen_fwd_host(
         ssd::StateIO io = io0;
         io.cache_indices = reinterpret_cast<const uint32_t *>(m + (b + 1) * 4);
         if (!ok(cudaStreamWaitEvent(stream, ds->in_done[k], 0)))
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
         const ssd_status_t st = ssd::scan_impl(
             ws + pl.y_off + a * rx, ws + pl.x_off + a * rx, ws + pl.dt_off + a * rdt, A,
             ws + pl.B_off + a * rb, ws + pl.C_off + a * rb, D, dt_bias, io,
@@ -389,16 +398,16 @@ ssd_status_t ssd_scan_varlen_fwd_host(
             static_cast<int64_t>(n), pc.batch(), nheads, head_dim, ngroups, dstate, chunk_size,
             dt_softplus, ws + pc.ws_off, pc.ws_bytes, stream_, nullptr, nullptr);
         if (st != SSD_OK)
-            return st;
+            return fail(st);
         if (!ok(cudaEventRecord(ds->scan_done[k], stream)) ||
             !ok(cudaStreamWaitEvent(ds->d2h, ds->scan_done[k], 0)))
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
         if (n > 0 && !ok(cudaMemcpyAsync(hy + a * rx, ws + pl.y_off + a * rx, n * rx,
                                          cudaMemcpyDeviceToHost, ds->d2h)))
-            return SSD_ERR_CUDA;
+            return fail(SSD_ERR_CUDA);
     }
     if (!ok(cudaEventRecord(ds->end, ds->d2h)) || !ok(cudaStreamWaitEvent(stream, ds->end, 0)))
-        return SSD_ERR_CUDA;
+        return fail(SSD_ERR_CUDA);
     return SSD_OK;
 }
 
