@@ -115,6 +115,30 @@ __host__ __device__ inline StageLayout stage_layout(int R, int N)
     return s;
 }
 
+// Packed fp32x2 arithmetic (sm_100 and later): two independent fp32
+// operations, each rounded to nearest even, in one instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // Sums each of v[0..K) over the L lanes (a power of two <= 32) of the aligned
 // lane group: a butterfly whose steps first halve the values a lane holds (it
 // keeps one half, its partner the other), then add the single value left.
@@ -244,14 +268,23 @@ __device__ __forceinline__ void consume(const ScanParams &p, const StageMeta &m,
                     for (int k = 0; k < NB; ++k)
                         b[k] = c[k] = 0.f;
                 }
+                // column pairs in packed fp32x2 instructions (the kernel is
+                // bound by instruction issue on sequences of several tokens)
+                const float2 dA2 = make_float2(da.y, da.y);
 #pragma unroll
                 for (int i = 0; i < RB; ++i) {
                     const float w = da.x * xv[i];
+                    const float2 w2 = make_float2(w, w);
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int k = 0; k < NB; ++k) {
-                        s[i][k] = fmaf(s[i][k], da.y, w * b[k]);
-                        part[u * RB + i] = fmaf(c[k], s[i][k], part[u * RB + i]);
+                    for (int k = 0; k < NB; k += 2) {
+                        const float2 wb = fmul2(w2, make_float2(b[k], b[k + 1]));
+                        const float2 sn = ffma2(make_float2(s[i][k], s[i][k + 1]), dA2, wb);
+                        s[i][k] = sn.x;
+                        s[i][k + 1] = sn.y;
+                        acc = ffma2(make_float2(c[k], c[k + 1]), sn, acc);
                     }
+                    part[u * RB + i] = acc.x + acc.y;
                 }
             }
         }
