@@ -135,3 +135,51 @@ def test_host_checks_reject_before_launch():
     torch.cuda.synchronize()
     assert torch.equal(d["pool"], before)
     assert not y.view(torch.int16).any()
+
+
+def test_back_to_back_calls_share_streams_and_ring():
+    """Six calls queued without a sync in between, alternating two workloads
+    and two workspaces: the library's shared copy streams, events and its
+    four-slot pinned ring (wrapped once here) must keep every call's inputs
+    and outputs apart.  Each result equals a device call on the same
+    inputs."""
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    ws_all = [W.make_workload("host_b2b_a", [700, 136, 0, 900], 4, 32, 2, 64, 128,
+                              max_slots=8, seed=520, has_init_p=0.5),
+              W.make_workload("host_b2b_b", [2048, 40, 1500], 4, 32, 2, 64, 128,
+                              max_slots=8, seed=521, has_init_p=0.5)]
+    refs = []
+    for w in ws_all:
+        y_dev, pool_dev, _, _ = run_cuda(w)
+        refs.append((y_dev.cpu(), pool_dev.cpu()))
+    staged = []
+    for w in ws_all:
+        h, _ = _host(w)
+        ws = pkg.alloc_host_workspace(h["qsl"], w.nheads, w.head_dim, w.ngroups, w.dstate,
+                                      w.chunk_size, 3)
+        staged.append((w, h, ws))
+    # every call's device arguments (a fresh pool each) and pinned y made up
+    # front, so that nothing between the calls waits for the device
+    args = []
+    for call in range(6):
+        w = staged[call % 2][0]
+        args.append((_host(w)[1],
+                     torch.full(w.x.shape, float("nan"), dtype=torch.bfloat16).pin_memory()))
+    torch.cuda.synchronize()
+    outs = []
+    for call in range(6):
+        w, h, ws = staged[call % 2]
+        d, y = args[call]
+        pkg.ssd_scan_varlen_fwd_host(y, h["x"], h["dt"], d["A"], h["B"], h["C"], d["D"],
+                                     d["dt_bias"], d["pool"], h["qsl"], h["hinit"], h["cidx"],
+                                     chunk_size=w.chunk_size, dt_softplus=w.dt_softplus,
+                                     pieces=3, workspace=ws)
+        outs.append((call % 2, y, d["pool"]))
+    torch.cuda.synchronize()
+    for k, y, pool in outs:
+        y_ref, pool_ref = refs[k]
+        # the pieces cut sequences, so the rounding differs slightly from one call
+        check_y(y_to_f64(y), y_to_f64(y_ref), what=f"call of workload {k}")
+        assert torch.allclose(pool.cpu(), pool_ref, rtol=1e-4, atol=1e-5)
+    for _, _, ws in staged:
+        assert pkg.ssd_scan_varlen_host_read_errors(ws) == 0
