@@ -183,3 +183,32 @@ def test_back_to_back_calls_share_streams_and_ring():
         assert torch.allclose(pool.cpu(), pool_ref, rtol=1e-4, atol=1e-5)
     for _, _, ws in staged:
         assert pkg.ssd_scan_varlen_host_read_errors(ws) == 0
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_empty_optionals_and_pageable_memory(pinned):
+    """D, dt_bias and has_initial_state absent (read as 0 / false), softplus
+    off, and (pinned=False) inputs and y in pageable host memory: the copies
+    then do not overlap, but the result is the same."""
+    import mamba_ssd_chunked_varlen_gb300 as pkg
+    w = W.make_workload("host_opt", [900, 0, 300, 7, 1200], 4, 32, 2, 64, 128, max_slots=8,
+                        seed=530, with_D=False, with_dt_bias=False, dt_softplus=False)
+    # no initial states in the workload: passing None for the flags means the same
+    assert w.D is None and w.dt_bias is None and not w.has_initial_state.any()
+    h, d = _host(w)
+    if not pinned:
+        h = {k: (v.clone() if v is not None else None) for k, v in h.items()}   # pageable
+        assert not h["x"].is_pinned()
+    y = torch.full(w.x.shape, float("nan"), dtype=torch.bfloat16)
+    if pinned:
+        y = y.pin_memory()
+    ws = pkg.alloc_host_workspace(h["qsl"], w.nheads, w.head_dim, w.ngroups, w.dstate,
+                                  w.chunk_size, 3)
+    pkg.ssd_scan_varlen_fwd_host(y, h["x"], h["dt"], d["A"], h["B"], h["C"], None, None,
+                                 d["pool"], h["qsl"], None, h["cidx"], chunk_size=w.chunk_size,
+                                 dt_softplus=False, pieces=3, workspace=ws)
+    assert pkg.ssd_scan_varlen_host_read_errors(ws) == 0
+    torch.cuda.synchronize()
+    y_ref, pool_ref = recurrence.run_workload(w)
+    check_y(y_to_f64(y), y_ref, what=f"pinned={pinned}")
+    check_slots(d["pool"].cpu().numpy(), pool_ref, w.ssm_pool, w)
