@@ -223,9 +223,10 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd_profiled(
  * exceeds it return SSD_ERR_TOO_LARGE without launching (64 MiB fits, for
  * example, one 4096-token sequence with nheads 16, head_dim 64, dstate 256).  The caller still passes every input and output.
  *
- * The first call on each device looks up that device's address of the array
- * (with the device current); make that first call before any stream capture.
- * It allocates nothing, now or later.  All calls on a device share the one
+ * Every call looks up the array's address on the current device
+ * (cudaGetSymbolAddress, which allocates nothing); the first call on a device
+ * may make CUDA load the library's device code there, so make that first call
+ * before any stream capture.  It allocates nothing, now or later.  All calls on a device share the one
  * array and it keeps the last call's contents (each call rewrites everything
  * it reads, so nothing needs clearing); calls whose execution overlaps on the
  * GPU (different streams, or different host threads) race on it and must be
@@ -292,7 +293,15 @@ SSD_API ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stre
  * a call waits on the host only if that buffer's copy from four calls
  * earlier has not run yet.  So the call cannot be captured into a CUDA
  * graph.  Device-side error flags are read with
- * ssd_scan_varlen_host_read_errors. */
+ * ssd_scan_varlen_host_read_errors.
+ *
+ * Every piece's host-side checks (and its tensor maps) run before the first
+ * copy is queued, so a host-side error status means, as for the other entry
+ * points, that nothing was copied, launched or written.  Only a failure of
+ * the CUDA runtime itself after the first copy was queued (SSD_ERR_CUDA) can
+ * leave earlier pieces launched: their y rows and slots are then written,
+ * and a sequence cut between a launched and a failed piece holds its
+ * mid-sequence state in its slot. */
 #define SSD_HOST_MAX_PIECES 8
 
 /* Bytes of workspace ssd_scan_varlen_fwd_host needs for this call (0 when
@@ -327,6 +336,16 @@ SSD_API ssd_status_t ssd_scan_varlen_fwd_host(
  * that used `workspace`.  Returns SSD_ERR_DEVICE if any flag is set. */
 SSD_API ssd_status_t ssd_scan_varlen_host_read_errors(const void *workspace, ssd_stream_t stream,
                                                       uint32_t *flags);
+
+/* Test hook of the bounded-wait failure path (the pages have no counterpart).
+ * With limit_ns > 0, every later call's chunk-state kernel (or fused scan
+ * kernel) also waits, after its input copies have landed, on an on-chip
+ * barrier that nothing completes; the wait gives up after limit_ns, the
+ * kernel records SSD_DEVERR_TIMEOUT, frees its tensor memory and returns, as
+ * it does when a real wait runs out (limit 1 s).  The outputs of such a call
+ * are incomplete.  0 (the default) turns the hook off.  Process-wide; not
+ * for production use. */
+SSD_API void ssd_scan_varlen_test_stall(uint32_t limit_ns);
 
 /* A static string naming a status code. */
 SSD_API const char *ssd_status_string(ssd_status_t status);

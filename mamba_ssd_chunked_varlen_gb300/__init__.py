@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     ssd_scan_varlen_fused_walk,
     ssd_scan_varlen_read_errors,
     ssd_scan_varlen_short_threshold,
+    ssd_scan_varlen_test_stall,
     ssd_scan_varlen_workspace_size,
     status_string,
 )

@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "ssd_scan_varlen_host_plan",
     "ssd_scan_varlen_fwd_host",
     "ssd_scan_varlen_host_read_errors",
+    "ssd_scan_varlen_test_stall",
 )
 
 HOST_MAX_PIECES = 8  # SSD_HOST_MAX_PIECES
@@ -103,6 +104,8 @@ def library() -> ctypes.CDLL:
     lib.ssd_scan_varlen_fwd_host.restype = ctypes.c_int
     lib.ssd_scan_varlen_fwd_host.argtypes = ([vp] * 12 + [i64, i32, i32, i32, i32, i32, i64, i32,
                                                           i32, i32] + [vp, sz, vp])
+    lib.ssd_scan_varlen_test_stall.restype = None
+    lib.ssd_scan_varlen_test_stall.argtypes = [ctypes.c_uint32]
     lib.ssd_scan_varlen_host_read_errors.restype = ctypes.c_int
     lib.ssd_scan_varlen_host_read_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     _lib = lib
@@ -344,6 +347,12 @@ def ssd_scan_varlen_read_errors(workspace, stream=None) -> int:
     if st not in (SSD_OK, 5):
         raise SSDError(st, "ssd_scan_varlen_read_errors")
     return int(flags.value)
+
+
+def ssd_scan_varlen_test_stall(limit_ns: int) -> None:
+    """Test hook: later calls wait on a never-completed on-chip barrier that
+    gives up after `limit_ns` (0 turns the hook off)."""
+    library().ssd_scan_varlen_test_stall(int(limit_ns))
 
 
 def alloc_workspace(total_len: int, batch: int, nheads: int, head_dim: int, ngroups: int,

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/ssd_scan.h"
@@ -71,6 +72,10 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Limit of the deliberate never-completed wait (ssd_scan_varlen_test_stall);
+// 0 outside the tests of the bounded-wait path.
+std::atomic<uint32_t> g_test_stall_ns{0};
 
 // Whether a call may hold sequences of at most kShortLenMax tokens (then the
 // short-sequence kernel runs): a batch of several sequences, or one sequence
@@ -184,7 +189,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                        int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim,
                        int32_t ngroups, int32_t dstate, int32_t chunk_size, int32_t dt_softplus,
                        void *workspace, size_t workspace_bytes, ssd_stream_t stream_,
-                       void *const *events, const TokenStrides *strides)
+                       void *const *events, const TokenStrides *strides, bool launch)
 {
     const ssd_status_t sz =
         check_sizes(total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size);
@@ -265,6 +270,7 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
     const bool walk = ssd::use_state_walk(total_len, batch, nheads, ngroups, head_dim, dstate, Qb);
     p.finish_single = (!walk && batch > 1) ? 1 : 0;
     p.max_chunks = static_cast<int32_t>(L.max_chunks);
+    p.test_stall_ns = g_test_stall_ns.load(std::memory_order_relaxed);
     p.hdr = reinterpret_cast<ssd::WsHeader *>(ws + L.header);
     p.seq_first = reinterpret_cast<int32_t *>(ws + L.seq_first);
     p.short_list = reinterpret_cast<ssd::SeqRec *>(ws + L.short_list);
@@ -312,6 +318,8 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
         if (!ok)
             return SSD_ERR_CUDA;
     }
+    if (!launch)
+        return SSD_OK;
 
     // Stage events (profiled entry point): before the first launch and after
     // each launch.  Between launches they also end the programmatic overlap.
@@ -443,6 +451,8 @@ ssd_status_t ssd_scan_varlen_fwd_profiled(
                           total_len, batch, nheads, head_dim, ngroups, dstate, chunk_size,
                           dt_softplus, workspace, workspace_bytes, stream, events);
 }
+
+void ssd_scan_varlen_test_stall(uint32_t limit_ns) { g_test_stall_ns.store(limit_ns); }
 
 ssd_status_t ssd_scan_varlen_read_errors(const void *workspace, ssd_stream_t stream_,
                                          uint32_t *flags)

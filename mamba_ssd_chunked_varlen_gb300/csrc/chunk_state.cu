@@ -59,7 +59,7 @@ __host__ __device__ inline K1Layout k1_layout(int NP, int n_mtiles, int HB)
     L.scratch = off;
     off += 64 * 4;
     L.bars = (off + 7) & ~7u;
-    off = L.bars + 4 * 8;
+    off = L.bars + 5 * 8;
     L.tmem_slot = off;
     off += 16;
     L.total = off;
@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
     uint64_t *bar_b = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *bar_x = bar_b + 1;
     uint64_t *bar_mma = bar_b + 2;   // one per state tile (n_mtiles <= 2)
+    uint64_t *bar_never = bar_b + 4;  // completed by nothing (the bounded-wait test)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
     float *s_part = reinterpret_cast<float *>(scratch + 40);  // 16 warp partials
 
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
         ptx::mbar_init(bar_x, 1);
         ptx::mbar_init(bar_mma, 1);
         ptx::mbar_init(bar_mma + 1, 1);
+        ptx::mbar_init(bar_never, 1);
         ptx::fence_barrier_init();
         // x rows of the block for the CTA's heads (MN-major, the layout of the
         // weighted operand, which is formed in place)
@@ -212,6 +214,11 @@ __global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
         SSD_TRACE_EV(0, 2);
 
     bool failed = !(ptx::mbar_wait(bar_x, 0, kWaitTimeoutNs) && ptx::mbar_wait(bar_b, 0, kWaitTimeoutNs));
+    // the tests of the bounded-wait path: once the loads have landed (no copy
+    // is in flight), one thread waits for a barrier that nothing completes;
+    // the wait gives up after test_stall_ns and the CTA takes the timeout path
+    if (p.test_stall_ns != 0 && tid == 0 && !failed)
+        failed = !ptx::mbar_wait(bar_never, 0, p.test_stall_ns);
     failed = __syncthreads_or(failed);
     if (tid == 0)
         SSD_TRACE_EV(0, 3);

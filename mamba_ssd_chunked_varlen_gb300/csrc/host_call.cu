@@ -309,6 +309,25 @@ ssd_status_t ssd_scan_varlen_fwd_host(
     uint8_t *hy = static_cast<uint8_t *>(y_host);
     const ssd::StateIO io0{ssm_pool, nullptr, max_slots, nullptr, nullptr, 0};
 
+    // every piece's host-side checks and tensor maps before anything is
+    // queued, so that a host-side error status means nothing was copied,
+    // launched or written
+    for (const Piece &pc : pl.pieces) {
+        const size_t a = static_cast<size_t>(pc.a), n = static_cast<size_t>(pc.e - pc.a);
+        const size_t b = pc.cidx.size();
+        uint8_t *m = ws + pc.meta_off;
+        ssd::StateIO io = io0;
+        io.cache_indices = reinterpret_cast<const uint32_t *>(m + (b + 1) * 4);
+        const ssd_status_t st = ssd::scan_impl(
+            ws + pl.y_off + a * rx, ws + pl.x_off + a * rx, ws + pl.dt_off + a * rdt, A,
+            ws + pl.B_off + a * rb, ws + pl.C_off + a * rb, D, dt_bias, io,
+            reinterpret_cast<const int32_t *>(m), m + (b + 1) * 4 + b * 4,
+            static_cast<int64_t>(n), pc.batch(), nheads, head_dim, ngroups, dstate, chunk_size,
+            dt_softplus, ws + pc.ws_off, pc.ws_bytes, stream_, nullptr, nullptr, false);
+        if (st != SSD_OK)
+            return st;
+    }
+
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceStreams *ds = nullptr;
     if (device_streams(&ds) != cudaSuccess)

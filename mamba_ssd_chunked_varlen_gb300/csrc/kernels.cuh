@@ -130,14 +130,18 @@ struct TokenStrides {
 };
 
 // The whole scan (argument checks, tensor maps, the three launches) on a
-// caller-provided scratch buffer; `events` (5 CUDA events) may be null.
+// caller-provided scratch buffer; `events` (5 CUDA events) may be null.  With
+// `launch` false it stops after every host-side check and tensor-map encoding
+// and launches nothing (the status is the one the call would return before
+// its first launch).
 ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, const void *B,
                        const void *C, const float *D, const float *dt_bias, const StateIO &io,
                        const int32_t *query_start_loc, const uint8_t *has_initial_state,
                        int64_t total_len, int32_t batch, int32_t nheads, int32_t head_dim,
                        int32_t ngroups, int32_t dstate, int32_t chunk_size, int32_t dt_softplus,
                        void *workspace, size_t workspace_bytes, ssd_stream_t stream,
-                       void *const *events, const TokenStrides *strides = nullptr);
+                       void *const *events, const TokenStrides *strides = nullptr,
+                       bool launch = true);
 
 inline int pad64(int v) { return (v + 63) / 64 * 64; }
 

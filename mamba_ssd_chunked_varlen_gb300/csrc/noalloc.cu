@@ -5,7 +5,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/ssd_scan.h"
 #include "kernels.cuh"
@@ -16,31 +15,18 @@ namespace {
 // that loads the library holds it until the process exits.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-
-std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current).  In host code the array's name is a
-// host-side stand-in, not a device address, so it is never passed directly.
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is a host-side stand-in, not a device address, so it is
+// never passed directly.  The address is looked up on every call (the lookup
+// allocates nothing): a cached address would go stale if the device's context
+// were reset and the library's device code loaded again at another address.
 cudaError_t scratch_for_current_device(void **out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess)
-            return e;
-        g_scratch_addr[dev] = ptr;
-    }
-    *out = g_scratch_addr[dev];
+    *out = ptr;
     return cudaSuccess;
 }
 

@@ -138,6 +138,9 @@ struct ScanParams {
     int32_t short_len;    // sequences of at most this many tokens go to the short-sequence
                           // kernel (the chunked kernels skip them); 0: none
     int32_t max_chunks;   // upper bound on the number of blocks
+    uint32_t test_stall_ns;   // 0; otherwise the chunk-state kernel (or the fused scan)
+                              // also waits on an mbarrier that nothing completes, with this
+                              // limit, so that the bounded-wait failure path runs (tests)
     // workspace regions
     WsHeader *hdr;
     int32_t *seq_first;   // (batch + 1): first block of each sequence, then the total

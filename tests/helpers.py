@@ -99,3 +99,29 @@ def check_slots(pool_gpu: np.ndarray, pool_ref: np.ndarray, pool_in: np.ndarray,
             assert np.array_equal(pool_gpu[s].view(np.uint32), pool_in[s].view(np.uint32)), \
                 f"{what}: untouched slot {s} changed"
     return worst
+
+
+def check_all_heads(w, y, pool, what="", span=16):
+    """Every head of every sequence against one full oracle run: y at the y
+    tolerance, written slots at the state tolerance, untouched slots
+    byte-identical.  The comparison runs over head ranges of at most `span`
+    heads at a time, each inside one B/C group when the group size allows,
+    which bounds the host memory of the temporaries on the largest
+    workloads."""
+    from oracle import recurrence
+    y_ref, pool_ref = recurrence.run_workload(w)
+    yg = y_to_f64(y) if hasattr(y, "cpu") else y
+    pg = pool.cpu().numpy() if hasattr(pool, "cpu") else pool
+    hpg = w.nheads // w.ngroups
+    step = hpg
+    while step > span and step % 2 == 0:
+        step //= 2
+    worst_y = worst_s = 0.0
+    for h0 in range(0, w.nheads, step):
+        h1 = min(w.nheads, h0 + step)
+        worst_y = max(worst_y, check_y(yg[:, h0:h1], y_ref[:, h0:h1],
+                                       what=f"{what} heads ({h0}, {h1})"))
+        worst_s = max(worst_s, check_slots(pg, pool_ref, w.ssm_pool, w, heads=(h0, h1),
+                                           what=f"{what} heads ({h0}, {h1})"))
+    return worst_y, worst_s
+

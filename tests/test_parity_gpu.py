@@ -12,7 +12,7 @@ import pytest
 from mamba_ssd_chunked_varlen_gb300 import workloads as W
 from oracle import recurrence
 
-from helpers import check_slots, check_y, run_cuda, to_device, y_to_f64
+from helpers import check_all_heads, check_slots, check_y, run_cuda, to_device, y_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -45,19 +45,17 @@ def test_workload_parity_full(name):
     _check_full(w, what=name)
 
 
-def test_nemotron_h_parity_sampled_heads():
-    """Full-size Nemotron-H-like workload, launched exactly as the benchmark
-    launches it; the oracle recomputes two head ranges (all sequences)."""
+def test_nemotron_h_parity_all_heads():
+    """Full-size Nemotron-H-like workload (8 B/C groups of 16 heads), launched
+    exactly as the benchmark launches it; every head of every sequence is
+    compared with the oracle, so every group of the grouped B/C map
+    (g = h // (nheads / ngroups)) is checked at full size, including the heads
+    on both sides of each group edge."""
     w = W.workload("nemotron_h")
     y, pool, _, ws = run_cuda(w)
     import mamba_ssd_chunked_varlen_gb300 as pkg
     assert pkg.ssd_scan_varlen_read_errors(ws) == 0
-    yg = y_to_f64(y)
-    pg = pool.cpu().numpy()
-    for heads in ((0, 8), (120, 128)):
-        y_ref, pool_ref = recurrence.run_workload(w, heads=heads)
-        check_y(yg[:, heads[0]:heads[1]], y_ref[:, heads[0]:heads[1]], what=f"heads {heads}")
-        check_slots(pg, pool_ref, w.ssm_pool, w, heads=heads, what=f"heads {heads}")
+    check_all_heads(w, y, pool, what="nemotron_h")
 
 
 @pytest.mark.parametrize("seed", range(16))

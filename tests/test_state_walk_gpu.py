@@ -4,7 +4,7 @@ sequences with many heads whose chunk states would exceed the L2.
 
 Every case first asserts that the library picks the walk for its sizes, so
 that these tests exercise it, then compares with the oracle (fp64 per-token
-recurrence) on sampled head ranges, every sequence: y at the y tolerance,
+recurrence) on every head, group by group, every sequence: y at the y tolerance,
 written slots at the state tolerance, untouched slots byte-identical.  The
 cases cover both tensor-memory column widths (64 and 128), two dstate tiles,
 64-token chunks, the bf16 pool, the separate-states form, and strided inputs
@@ -21,7 +21,8 @@ import pytest
 from mamba_ssd_chunked_varlen_gb300 import workloads as W
 from oracle import recurrence
 
-from helpers import STATE_REL_L2, check_slots, check_y, run_cuda, to_device, y_to_f64
+from helpers import (STATE_REL_L2, check_all_heads, check_slots, check_y, run_cuda,
+                     to_device, y_to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,16 +53,14 @@ def _assert_walk(w):
 
 
 def _head_ranges(w):
-    return ((0, 2), (w.nheads - 2, w.nheads))
+    """Head ranges compared with the oracle: every head, one B/C group at a time."""
+    hpg = w.nheads // w.ngroups
+    return tuple((h, h + hpg) for h in range(0, w.nheads, hpg))
 
 
 def _check_sampled(w, y, pool, what):
-    yg = y_to_f64(y)
-    pg = pool.cpu().numpy() if hasattr(pool, "cpu") else pool
-    for heads in _head_ranges(w):
-        y_ref, pool_ref = recurrence.run_workload(w, heads=heads)
-        check_y(yg[:, heads[0]:heads[1]], y_ref[:, heads[0]:heads[1]], what=f"{what} heads {heads}")
-        check_slots(pg, pool_ref, w.ssm_pool, w, heads=heads, what=f"{what} heads {heads}")
+    """Every head of every sequence (one oracle run, compared group by group)."""
+    check_all_heads(w, y, pool, what=what)
 
 
 @pytest.mark.parametrize("shape", [
@@ -104,8 +103,8 @@ def test_walk_bf16_pool():
     got = W.bf16_bits_to_f32(got_bits).astype(np.float64)
     yg = y_to_f64(y)
     written = set(int(s) for s in w.cache_indices)
+    y_ref, pool_ref = recurrence.run_workload(wr)
     for heads in _head_ranges(w):
-        y_ref, pool_ref = recurrence.run_workload(wr, heads=heads)
         check_y(yg[:, heads[0]:heads[1]], y_ref[:, heads[0]:heads[1]], what=f"bf16 pool {heads}")
         for s in written:
             ref = pool_ref[s][heads[0]:heads[1]].astype(np.float64)
@@ -143,8 +142,8 @@ def test_walk_states_form():
     yg = y_to_f64(y)
     fin = final.cpu().numpy()
     assert np.all(np.isfinite(fin)), "final_states not fully written"
+    y_ref, pool_ref = recurrence.run_workload(wr)
     for heads in _head_ranges(w):
-        y_ref, pool_ref = recurrence.run_workload(wr, heads=heads)
         check_y(yg[:, heads[0]:heads[1]], y_ref[:, heads[0]:heads[1]], what=f"states {heads}")
         for b, s in enumerate(w.cache_indices):
             ref = pool_ref[int(s)][heads[0]:heads[1]].astype(np.float64)
@@ -287,8 +286,8 @@ def test_walk_bad_cache_index():
     wr.has_initial_state = w.has_initial_state.copy()
     wr.has_initial_state[1] = 0
     yg = y_to_f64(y)
+    y_ref, pool_ref = recurrence.run_workload(wr)
     for heads in _head_ranges(w):
-        y_ref, pool_ref = recurrence.run_workload(wr, heads=heads)
         check_y(yg[:, heads[0]:heads[1]], y_ref[:, heads[0]:heads[1]], what=f"bad slot {heads}")
         for b in (0, 2):
             s = int(w.cache_indices[b])
