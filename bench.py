@@ -7,8 +7,9 @@ several sequences) on the kernelindex-shaped workload: one
 4096-token sequence, nheads=16, head_dim=64, ngroups=1, dstate=256, chunk 256
 (the head/state shape of the kernelindex "Mamba chunk scan with segsum"
 suite, whose cases are not published).  Inputs are seeded synthetic data
-resident in HBM; the L2 cache is flushed (a 512 MB write) before every timed
-call, because this workload's 22 MB of inputs would otherwise stay in the
+resident in HBM; the L2 cache is emptied before every timed call (a 512 MB
+write, then a read of a separate 512 MB buffer so that the call finds clean
+lines), because this workload's 22 MB of inputs would otherwise stay in the
 129 MB L2.
 
 Prints ONE JSON line on rank 0:
@@ -20,7 +21,14 @@ Prints ONE JSON line on rank 0:
               the step's inputs, the scan and the device -> host copy of y,
               overlapped piece by piece, all inside the timed region)
   roofline    the dominant kernel's achieved bytes (or flops) per launch over
-              its event-timed duration, against the measured peak
+              its event-timed duration, against the measured peak; `kernels`
+              has the same for every kernel the call launches
+  harness_floor_us  events around nothing, and around one tiny launch, after
+              the same flush: what no call measured this way can go below
+  us_per_call_write_only_flush  the call after a write-only flush (the L2
+              left full of modified lines), the flush of earlier measurements
+  workloads   the ragged, Nemotron-H-like, serving-mix and decode workloads,
+              timed the same way with fewer steps
   cpu_baseline  the fp64 oracle on this machine's host cores (a bounded sample)
 
 `--impl reference` times the oracle instead (the reference arm), on the same
@@ -305,6 +313,158 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+class L2Flush:
+    """Empties the L2 before a timed call without leaving it full of modified
+    lines: a 512 MB write (evicts everything), then a read of a separate 512 MB
+    buffer (replaces the written lines with clean ones, so that the call does
+    not pay for writing them back).  Both run outside the timed events."""
+
+    def __init__(self, dev, write_only: bool = False):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.r = None if write_only else torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32,
+                                                    device=dev)
+
+    def __call__(self, k: int):
+        self.w.fill_(k)
+        if self.r is not None:
+            self.r.sum()
+
+    def describe(self) -> str:
+        if self.r is None:
+            return f"flushed before every timed call ({L2_FLUSH_BYTES >> 20} MB write)"
+        return (f"flushed before every timed call ({L2_FLUSH_BYTES >> 20} MB write, then a "
+                f"read of a separate {L2_FLUSH_BYTES >> 20} MB buffer: the call starts with "
+                f"clean cold lines)")
+
+
+def time_calls(call, flush, K: int, stream) -> list:
+    """CUDA-event times (µs) of K calls on `stream`, each after `flush`."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for k in range(K):
+        flush(k)
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+
+def launched_stages(pkg, w) -> list:
+    """The stages a call of these sizes launches kernels for, in order."""
+    T = w.total_len
+    walk = pkg.ssd_scan_varlen_fused_walk(T, w.batch, w.nheads, w.head_dim, w.ngroups,
+                                          w.dstate, w.chunk_size)
+    out = []
+    if T > 0:
+        out.append("chunk_state")
+        if not walk:
+            out.append("state_passing")
+        out.append("chunk_scan")
+    if pkg.ssd_scan_varlen_short_threshold(T, w.batch) > 0:
+        out.append("short_scan")
+    return out
+
+
+def stage_times(pkg, w, d, y, ws, flush, Kp: int, stream) -> dict:
+    """Per-stage event times (µs, mean of Kp profiled calls: events between the
+    launches, programmatic overlap off) of the stages that launch a kernel."""
+    import torch
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(Kp)]
+    for k in range(Kp):
+        flush(k)
+        pkg.ssd_scan_varlen_fwd_profiled(
+            y, d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], d["pool"],
+            d["qsl"], d["hinit"], d["cidx"], chunk_size=w.chunk_size, dt_softplus=w.dt_softplus,
+            workspace=ws, stream=stream, events=sev[k])
+    torch.cuda.synchronize()
+    live = launched_stages(pkg, w)
+    return {s: sum(sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(Kp)) / Kp * 1e3
+            for i, s in enumerate(STAGES) if s in live}
+
+
+def kernel_roofline(stage: str, us: float, model: dict, peaks: dict) -> dict:
+    """A stage's algorithmic bytes or flops per launch over its event time,
+    against the measured peak, whichever bound is the larger time."""
+    st = model["stages"][stage]
+    t_s = us * 1e-6
+    t_bytes = st["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_flops = st["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_flops > t_bytes:
+        achieved = st["flops"] / t_s / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "us_per_launch": round(us, 3)}
+    achieved = st["bytes"] / t_s / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "us_per_launch": round(us, 3)}
+
+
+def scan_call(pkg, w, d, y, ws, stream):
+    """The in-place device-buffer call on workload `w` with inputs `d`."""
+    def call():
+        pkg.ssd_scan_varlen_fwd(y, d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"],
+                                d["pool"], d["qsl"], d["hinit"], d["cidx"],
+                                chunk_size=w.chunk_size, dt_softplus=w.dt_softplus,
+                                workspace=ws, stream=stream)
+    return call
+
+
+def other_workloads(pkg, names, dev, stream, flush, peaks, steps: int, local: int) -> dict:
+    """The other workloads of this op, timed the same way as the headline
+    (clean L2 flush before each call, CUDA events), fewer steps; inputs drawn on
+    the device (seeded) with the workloads' shapes and value recipe."""
+    import torch
+    out = {}
+    for name in names:
+        w = W.device_workload(name, dev)
+        d = w.dev
+        T = w.total_len
+        y = torch.empty((T, w.nheads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        ws = pkg.alloc_workspace(T, w.batch, w.nheads, w.head_dim, w.ngroups, w.dstate,
+                                 w.chunk_size, device=dev)
+        walk = pkg.ssd_scan_varlen_fused_walk(T, w.batch, w.nheads, w.head_dim, w.ngroups,
+                                              w.dstate, w.chunk_size)
+        model = work_model(w, pkg.ssd_scan_varlen_short_threshold(T, w.batch), walk)
+        call = scan_call(pkg, w, d, y, ws, stream)
+        for k in range(3):
+            flush(k)
+            call()
+        flags = pkg.ssd_scan_varlen_read_errors(ws, stream)
+        if flags:
+            raise RuntimeError(f"{name}: device error flags {flags:#x}")
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.1)
+        torch.cuda.synchronize(dev)
+        ts = time_calls(call, flush, steps, stream)
+        clocks = sampler.stop()
+        us = sum(ts) / len(ts)
+        stg = stage_times(pkg, w, d, y, ws, flush, max(5, steps // 2), stream)
+        t_roof = max(model["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                     model["flops"] / (peaks["bf16_tflops"] * 1e12))
+        dom = max(stg, key=stg.get)
+        out[name] = {
+            "total_len": T, "batch": w.batch, "us_per_call": round(us, 3),
+            "us_per_call_median": round(statistics.median(ts), 3),
+            "tokens_per_s": round(T / (us * 1e-6), 1),
+            "roofline_call": {"t_roofline_us": round(t_roof * 1e6, 3),
+                              "frac": round(t_roof / (us * 1e-6), 4),
+                              "bytes": model["bytes"], "flops": model["flops"]},
+            "kernels": {s: kernel_roofline(s, stg[s], model, peaks) for s in stg},
+            "dominant": stage_kernel(dom, walk),
+            "state_kernels": "fused walk" if walk else "chunk_state + state_passing",
+            "steps": steps, "clocks": clocks,
+            "data": "synthetic, drawn on the device (seeded torch generator, same recipe)"}
+        del d, y, ws, w
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
     import mamba_ssd_chunked_varlen_gb300 as pkg
@@ -333,7 +493,7 @@ def run_ours(args, rank, world, local):
     y = torch.empty(w.x.shape, dtype=torch.bfloat16, device=dev)
     ws = pkg.alloc_workspace(T, w.batch, w.nheads, w.head_dim, w.ngroups, w.dstate,
                              w.chunk_size, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
 
     if args.form == "states":
         # the separate-state-array form: initial_states are the workload's pool
@@ -386,8 +546,8 @@ def run_ours(args, rank, world, local):
                                 dt_softplus=w.dt_softplus, workspace=ws, stream=stream)
 
     # ---- warm-up
-    for _ in range(args.warmup):
-        flush.fill_(1)
+    for k in range(args.warmup):
+        flush(k)
         call()
     flags = pkg.ssd_scan_varlen_read_errors(ws, stream)
     if flags:
@@ -395,40 +555,34 @@ def run_ours(args, rank, world, local):
 
     # ---- timed region: K calls, L2 flushed before each, events around each call
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.1)
     dist_barrier()
     torch.cuda.synchronize(dev)
-    for k in range(K):
-        flush.fill_(k)
-        ev[k][0].record(stream)
-        call()
-        ev[k][1].record(stream)
-    torch.cuda.synchronize(dev)
+    times_us = time_calls(call, flush, K, stream)
     dist_barrier()
     clocks = sampler.stop()
-    times_ms = [a.elapsed_time(b) for a, b in ev]
-    mean_ms = sum(times_ms) / K
+    mean_ms = sum(times_us) / K * 1e-3
     mean_ms_all = dist_reduce(mean_ms, "max")
     tokens_all = T * world
     value = tokens_all / (mean_ms_all * 1e-3)
 
+    # ---- the same call after the write-only flush of earlier measurements
+    # (the L2 full of modified lines that the call then writes back), and the
+    # floor of the harness: events around nothing and around one tiny launch,
+    # after the same clean flush
+    Kf = min(K, 300)
+    dirty = L2Flush(dev, write_only=True)
+    us_dirty = statistics.mean(time_calls(call, dirty, Kf, stream))
+    del dirty
+    tiny = torch.zeros(1, device=dev)
+    floor = {"empty_events": round(statistics.mean(time_calls(lambda: None, flush, Kf, stream)), 3),
+             "one_tiny_launch": round(statistics.mean(time_calls(lambda: tiny.add_(1), flush, Kf,
+                                                                 stream)), 3)}
+
     # ---- per-stage attribution (stage events between the launches)
-    Kp = min(K, 500)
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
-           for _ in range(Kp)]
-    for k in range(Kp):
-        flush.fill_(k)
-        pkg.ssd_scan_varlen_fwd_profiled(
-            y, d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], d["pool"], d["qsl"],
-            d["hinit"], d["cidx"], chunk_size=w.chunk_size, dt_softplus=w.dt_softplus,
-            workspace=ws, stream=stream, events=sev[k])
-    torch.cuda.synchronize(dev)
-    stage_ms = {s: sum(sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(Kp)) / Kp
-                for i, s in enumerate(STAGES)}
+    stage_us = stage_times(pkg, w, d, y, ws, flush, min(K, 500), stream)
 
     # ---- end to end through the public API with host buffers
     Ke = min(K, 500)
@@ -440,8 +594,6 @@ def run_ours(args, rank, world, local):
     y_host = torch.empty(w.x.shape, dtype=torch.int16).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = y_host.numel() * 2
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(Ke)]
     # the in-place form goes through the host-buffer entry point (its copies
     # in, the scan and y's copy out overlap piece by piece); the other forms
     # copy the inputs, call the device entry point and copy y back
@@ -454,9 +606,8 @@ def run_ours(args, rank, world, local):
         e2e_pieces = len(pkg.ssd_scan_varlen_host_plan(
             host["qsl"], w.nheads, w.head_dim, w.ngroups, w.dstate, w.chunk_size,
             args.e2e_pieces)) + 1
-    for k in range(Ke):
-        flush.fill_(k)
-        eev[k][0].record(stream)
+
+    def e2e_call():
         if host_call:
             pkg.ssd_scan_varlen_fwd_host(
                 y_hb, hb["x"], hb["dt"], d["A"], hb["B"], hb["C"], d["D"], d["dt_bias"],
@@ -469,36 +620,28 @@ def run_ours(args, rank, world, local):
                         dev_in[key]) for key in dev_in}
             call(dd=dd)
             y_host.copy_(y.view(torch.int16), non_blocking=True)
-        eev[k][1].record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / Ke
+
+    e2e_ms = statistics.mean(time_calls(e2e_call, flush, Ke, stream)) * 1e-3
     e2e_ms_all = dist_reduce(e2e_ms, "max")
     flags = (pkg.ssd_scan_varlen_host_read_errors(hws, stream) if host_call else 0) | \
         pkg.ssd_scan_varlen_read_errors(ws, stream)
     if flags:
         raise RuntimeError(f"device error flags {flags:#x}")
 
-    # ---- roofline of the dominant kernel
+    # ---- roofline of every launched kernel; the one with the longest event time
     peaks = load_peaks()
-    dom = max(STAGES, key=lambda s: stage_ms[s])
-    st = model["stages"][dom]
-    t_s = stage_ms[dom] * 1e-3
-    t_bytes = st["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_flops = st["flops"] / (peaks["bf16_tflops"] * 1e12)
-    if t_flops > t_bytes:
-        achieved = st["flops"] / t_s / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
-    else:
-        achieved = st["bytes"] / t_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roof["traffic"] = measured_traffic(stage_kernel(dom, walk), args.workload)
+    kernels = {s: kernel_roofline(s, stage_us[s], model, peaks) for s in stage_us}
+    dom = max(stage_us, key=stage_us.get)
+    roof = dict(kernels[dom])
     roof["kernel"] = stage_kernel(dom, walk)
+    roof["traffic"] = measured_traffic(stage_kernel(dom, walk), args.workload)
+    roof["traffic_source"] = (
+        "ncu dram__bytes_read.sum + dram__bytes_write.sum of one cold-cache replay of the "
+        "kernel's current source (profiles/dram_traffic.md)" if roof["traffic"] is not None
+        else "no ncu capture of the kernel's current source")
     roof["peak_source"] = peaks["source"] + " (burst)"
-    roof["algorithmic_bytes"] = st["bytes"]
-    roof["algorithmic_flops"] = st["flops"]
-    roof["us_per_launch"] = round(stage_ms[dom] * 1e3, 3)
+    roof["algorithmic_bytes"] = model["stages"][dom]["bytes"]
+    roof["algorithmic_flops"] = model["stages"][dom]["flops"]
     t_roof = max(model["bytes"] / (peaks["hbm_gbs"] * 1e9),
                  model["flops"] / (peaks["bf16_tflops"] * 1e12))
 
@@ -510,17 +653,20 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "total_len": T, "batch": w.batch, "nheads": w.nheads,
                    "head_dim": w.head_dim, "ngroups": w.ngroups, "dstate": w.dstate,
                    "chunk_size": w.chunk_size, "chunks": model["chunks"], "form": args.form,
-                   "l2": f"flushed before every timed call ({L2_FLUSH_BYTES >> 20} MB write)",
-                   "state_kernels": ("fused walk (chunk_state stage; state_passing empty)"
+                   "l2": flush.describe(),
+                   "state_kernels": ("fused walk (chunk_state stage; no state_passing launch)"
                                      if walk else "chunk_state + state_passing"),
                    "parallelism": f"replicas x{world}"},
         "us_per_call": round(mean_ms_all * 1e3, 3),
-        "us_per_call_median": round(statistics.median(times_ms) * 1e3, 3),
+        "us_per_call_median": round(statistics.median(times_us), 3),
+        "us_per_call_write_only_flush": round(us_dirty, 3),
+        "harness_floor_us": floor,
         "roofline": roof,
         "roofline_call": {"t_roofline_us": round(t_roof * 1e6, 3),
                           "frac": round(t_roof / (mean_ms_all * 1e-3), 4),
                           "bytes": model["bytes"], "flops": model["flops"]},
-        "stages_us": {s: round(stage_ms[s] * 1e3, 3) for s in STAGES},
+        "kernels": kernels,
+        "stages_us": {s: round(v, 3) for s, v in stage_us.items()},
         "e2e": {"value": round(tokens_all / (e2e_ms_all * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e2e_ms_all * 1e3, 3),
@@ -530,6 +676,12 @@ def run_ours(args, rank, world, local):
                                                              w.ngroups, w.dstate, w.chunk_size),
         "clocks": clocks,
     }
+    if args.other_workloads and args.form == "inplace":
+        names = [n for n in ("ragged", "nemotron_h", "serving_mix", "decode") if n != w.name]
+        del d, y, ws
+        torch.cuda.empty_cache()
+        result["workloads"] = other_workloads(pkg, names, dev, stream, flush, peaks,
+                                              args.other_steps, local)
     return result, w
 
 
@@ -559,6 +711,13 @@ def oracle_time(w, budget_s: float, min_reps: int = 1, max_reps: int = 50):
     sample = (f"{w.name}: {w.total_len} tokens x {heads}/{w.nheads} heads per call, "
               f"{len(times)} calls, median {med * 1e3:.1f} ms")
     return value, cores, sample, med, heads
+
+
+def host_cores() -> dict:
+    """The machine's host cores and the OpenMP threads the oracle may use."""
+    from oracle import recurrence
+    return {"host_cores": os.cpu_count(), "omp_threads": recurrence.max_threads(),
+            "omp_num_threads_env": os.environ.get("OMP_NUM_THREADS")}
 
 
 def run_reference(args, rank, world):
@@ -596,8 +755,8 @@ def run_reference(args, rank, world):
                    "dstate": w.dstate, "chunk_size": w.chunk_size,
                    "parallelism": "host cores (OpenMP over sequence x head)"},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores,
-                         "kind": "oracle", "sample": sample},
+        "cpu_baseline": dict({"value": round(value, 1), "unit": UNIT, "cores": cores,
+                              "kind": "oracle", "sample": sample}, **host_cores()),
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -623,6 +782,11 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--other-workloads", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time the ragged, Nemotron-H-like, serving-mix and decode "
+                         "workloads (the 'workloads' key; in-place form only)")
+    ap.add_argument("--other-steps", type=int, default=40,
+                    help="timed calls per other workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -640,8 +804,9 @@ def main(argv=None):
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             value, cores, sample, _, _ = oracle_time(w, args.cpu_budget)
-            result["cpu_baseline"] = {"value": round(value, 1), "unit": UNIT, "cores": cores,
-                                      "kind": "oracle", "sample": sample}
+            result["cpu_baseline"] = dict({"value": round(value, 1), "unit": UNIT,
+                                           "cores": cores, "kind": "oracle", "sample": sample},
+                                          **host_cores())
         else:
             result["cpu_baseline"] = None
         print(json.dumps(result), flush=True)

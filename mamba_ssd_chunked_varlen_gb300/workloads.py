@@ -200,30 +200,113 @@ def workload(name: str, seed: Optional[int] = None) -> Workload:
     For tiny and kernelindex the pool has 4 slots and one random slot is
     written, so that the untouched-slot check has something to check.
     """
+    sp = workload_spec(name, seed)
+    return make_workload(name, sp["lens"], sp["nheads"], sp["head_dim"], sp["ngroups"],
+                         sp["dstate"], sp["chunk_size"], max_slots=sp["max_slots"],
+                         seed=sp["seed"], has_init_p=sp["has_init_p"])
+
+
+def workload_spec(name: str, seed: Optional[int] = None) -> dict:
+    """Sizes, sequence lengths, pool size, seed and initial-state probability
+    of a standard workload (see `workload`), without drawing its arrays."""
     idx = WORKLOADS.index(name)
     seed = idx if seed is None else seed
+
+    def spec(lens, H, P, G, N, Q, max_slots, has_init_p=0.0):
+        return dict(lens=[int(v) for v in lens], nheads=H, head_dim=P, ngroups=G, dstate=N,
+                    chunk_size=Q, max_slots=max_slots, seed=seed, has_init_p=has_init_p)
+
     if name == "tiny":
-        return make_workload(name, [512], 4, 32, 1, 32, 64, max_slots=4, seed=seed)
+        return spec([512], 4, 32, 1, 32, 64, 4)
     if name == "kernelindex":
-        return make_workload(name, [4096], 16, 64, 1, 256, 256, max_slots=4, seed=seed)
+        return spec([4096], 16, 64, 1, 256, 256, 4)
     if name == "ragged":
         lens = _ragged_lengths(np.random.default_rng([seed, 1]), 8, 1, 4096, 256)
-        return make_workload(name, lens, 16, 64, 1, 256, 256, max_slots=64, seed=seed,
-                             has_init_p=0.5)
+        return spec(lens, 16, 64, 1, 256, 256, 64, 0.5)
     if name == "nemotron_h":
-        return make_workload(name, [8192] * 4, 128, 64, 8, 128, 256, max_slots=16,
-                             seed=seed, has_init_p=1.0)
+        return spec([8192] * 4, 128, 64, 8, 128, 256, 16, 1.0)
     if name == "serving_mix":
         lens = np.random.default_rng([seed, 1]).geometric(1.0 / 64.0, 256)
-        return make_workload(name, lens, 64, 64, 1, 128, 256, max_slots=512, seed=seed,
-                             has_init_p=0.8)
+        return spec(lens, 64, 64, 1, 128, 256, 512, 0.8)
     if name == "nemotron_h_2k":
-        return make_workload(name, [2048] * 4, 128, 64, 8, 128, 256, max_slots=16,
-                             seed=seed, has_init_p=1.0)
+        return spec([2048] * 4, 128, 64, 8, 128, 256, 16, 1.0)
     if name == "decode":
-        return make_workload(name, [1] * 256, 64, 64, 1, 128, 256, max_slots=512, seed=seed,
-                             has_init_p=1.0)
+        return spec([1] * 256, 64, 64, 1, 128, 256, 512, 1.0)
     raise KeyError(name)
+
+
+@dataclasses.dataclass
+class DeviceWorkload:
+    """A workload drawn directly on a CUDA device (for timing large workloads
+    without a host round trip): the sizes and small host arrays of `Workload`
+    plus the device tensors in `dev` (x, dt, A, B, C, D, dt_bias, pool, qsl,
+    hinit, cidx).  Same value recipe as `make_workload`, drawn by torch's
+    seeded device generator instead of NumPy, so the values differ from the
+    host workload of the same name."""
+
+    name: str
+    nheads: int
+    head_dim: int
+    ngroups: int
+    dstate: int
+    chunk_size: int
+    query_start_loc: np.ndarray
+    has_initial_state: np.ndarray
+    cache_indices: np.ndarray
+    dev: dict
+    dt_softplus: bool = True
+
+    @property
+    def total_len(self) -> int:
+        return int(self.query_start_loc[-1])
+
+    @property
+    def batch(self) -> int:
+        return int(self.query_start_loc.shape[0] - 1)
+
+    @property
+    def seq_lens(self) -> np.ndarray:
+        return np.diff(self.query_start_loc.astype(np.int64))
+
+
+def device_workload(name: str, device, seed: Optional[int] = None) -> DeviceWorkload:
+    """The standard workload `name` drawn on `device` (see DeviceWorkload)."""
+    import torch
+
+    sp = workload_spec(name, seed)
+    H, P, G, N = sp["nheads"], sp["head_dim"], sp["ngroups"], sp["dstate"]
+    lens = np.asarray(sp["lens"], dtype=np.int64)
+    batch = int(lens.shape[0])
+    T = int(lens.sum())
+    qsl = np.zeros(batch + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(lens)
+    rng = np.random.default_rng([sp["seed"], 11])
+    A = (-np.exp(rng.uniform(np.log(1.0), np.log(16.0), H))).astype(np.float32)
+    u = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), H))
+    dt_bias = np.log(np.expm1(u)).astype(np.float32)
+    D = rng.standard_normal(H).astype(np.float32)
+    cidx = rng.permutation(sp["max_slots"])[:batch].astype(np.uint32)
+    hinit = ((rng.random(batch) < sp["has_init_p"]) if sp["has_init_p"] > 0.0
+             else np.zeros(batch, bool)).astype(np.uint8)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(sp["seed"]) * 7919 + 17)
+
+    def normal(shape, std=1.0):
+        return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std)
+
+    dev = dict(
+        x=normal((T, H, P)).to(torch.bfloat16),
+        dt=normal((T, H), 0.5).to(torch.bfloat16),
+        B=normal((T, G, N)).to(torch.bfloat16),
+        C=normal((T, G, N)).to(torch.bfloat16),
+        pool=normal((sp["max_slots"], H, P, N), 0.1),
+        A=torch.from_numpy(A).to(device), D=torch.from_numpy(D).to(device),
+        dt_bias=torch.from_numpy(dt_bias).to(device),
+        qsl=torch.from_numpy(qsl).to(device), hinit=torch.from_numpy(hinit).to(device),
+        cidx=torch.from_numpy(cidx.astype(np.int32)).to(device))
+    return DeviceWorkload(name=name, nheads=H, head_dim=P, ngroups=G, dstate=N,
+                          chunk_size=sp["chunk_size"], query_start_loc=qsl,
+                          has_initial_state=hinit, cache_indices=cidx, dev=dev)
 
 
 def random_small_workload(seed: int, max_total: int = 600) -> Workload:
