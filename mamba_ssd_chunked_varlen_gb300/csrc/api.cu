@@ -280,7 +280,8 @@ ssd_status_t scan_impl(void *y, const void *x, const void *dt, const float *A, c
                   ? reinterpret_cast<ssd::BlockEntry *>(ws + L.table)
                   : nullptr;
     p.decay = reinterpret_cast<float *>(ws + L.decay);
-    p.schunk = reinterpret_cast<float *>(ws + L.schunk);
+    p.schunk = reinterpret_cast<__half *>(ws + L.schunk);
+    p.sexp = reinterpret_cast<int8_t *>(ws + L.sexp);
     p.sprev = reinterpret_cast<__nv_bfloat16 *>(ws + L.sprev);
 
     ssd::ChunkStateMaps m1;

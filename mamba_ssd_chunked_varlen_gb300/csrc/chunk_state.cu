@@ -23,7 +23,9 @@
 // CTA (0,0) writes the per-sequence first-block table and resets the error word.
 //
 // Block states are stored [block][head][p][n] like the pool's slots, so the
-// state-passing kernel reads and writes both with the same coalesced pattern.
+// state-passing kernel reads and writes both with the same coalesced pattern;
+// they cross the workspace as fp16 with a power-of-two exponent per 16
+// consecutive p (state_group_exp), half the bytes of fp32.
 #include "kernels.cuh"
 #include "sm100_ptx.cuh"
 #include "ssd_device.cuh"
@@ -343,14 +345,22 @@ __global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
                     float v[16];
                     ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * NP + c, v);
                     if (n < p.N && c < width) {
-                        // 16 columns never straddle two heads (head_dim % 16 == 0); a
-                        // warp writes 32 consecutive n of one p: 128 contiguous bytes
+                        // 16 columns never straddle two heads (head_dim % 16 == 0) and
+                        // start on a multiple of 16 of p: one exponent group.  A warp
+                        // writes 32 consecutive n of one p: 64 contiguous bytes
                         const int hh = c / p.P, p0 = c % p.P;
-                        float *dst = p.schunk +
-                                     ((static_cast<int64_t>(blk) * p.H + h0 + hh) * p.P + p0) * p.N + n;
+                        const int64_t hrow = static_cast<int64_t>(blk) * p.H + h0 + hh;
+                        __half *dst = p.schunk + (hrow * p.P + p0) * p.N + n;
+                        float m = 0.f;
 #pragma unroll
                         for (int k = 0; k < 16; ++k)
-                            dst[static_cast<int64_t>(k) * p.N] = v[k];
+                            m = fmaxf(m, fabsf(v[k]));
+                        const int ke = state_group_exp(m);
+                        const float sc = pow2i(ke);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            dst[static_cast<int64_t>(k) * p.N] = __float2half_rn(v[k] * sc);
+                        p.sexp[(hrow * (p.P / 16) + p0 / 16) * p.N + n] = static_cast<int8_t>(ke);
                     }
                 }
                 continue;
@@ -384,6 +394,10 @@ __global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
                     const int c = cq * ncols + ci * 16;
                     float v[16];
                     ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * NP + c, v);
+                    // the block state rounded as it crosses the workspace for a longer
+                    // sequence (fp16 with the group's exponent), so that a sequence
+                    // finished here and one continued from its slot see the same values
+                    round_state_group(v);
                     if (n < p.N && c < width) {
                         const int hh = c / p.P, p0 = c % p.P;
                         const int64_t row = (static_cast<int64_t>(blk) * p.H + h0 + hh) * p.P + p0;

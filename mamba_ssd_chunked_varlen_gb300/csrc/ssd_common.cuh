@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace ssd {
@@ -31,7 +32,7 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 // Byte offsets of the workspace regions; every region is 256-byte aligned.
 struct WsLayout {
     int64_t max_chunks;
-    size_t header, seq_first, short_list, long_list, table, decay, schunk, sprev, total;
+    size_t header, seq_first, short_list, long_list, table, decay, schunk, sexp, sprev, total;
 };
 
 // Batches of more sequences than this map their blocks once, in a kernel of
@@ -99,7 +100,9 @@ __host__ __device__ inline WsLayout ws_layout(int64_t T, int32_t batch, int32_t 
     L.decay = off;
     off = align256(off + sizeof(float) * mc * H);
     L.schunk = off;
-    off = align256(off + sizeof(float) * mc * H * P * N);
+    off = align256(off + sizeof(__half) * mc * H * P * N);
+    L.sexp = off;
+    off = align256(off + sizeof(int8_t) * mc * H * (P / 16) * N);
     L.sprev = off;
     off = align256(off + sizeof(__nv_bfloat16) * mc * H * P * N);
     L.total = off;
@@ -150,7 +153,9 @@ struct ScanParams {
     BlockEntry *table;    // per block, when the block-map kernel runs; else null (each
                           // CTA maps its own block)
     float *decay;         // [block][head] exp(sum of A*dt over the block)
-    float *schunk;        // [block][head][P][N] block states (zero initial state)
+    __half *schunk;       // [block][head][P][N] block states (zero initial state) in fp16,
+                          // each scaled by 2^sexp of its group of 16 consecutive p
+    int8_t *sexp;         // [block][head][P/16][N] those exponents
     __nv_bfloat16 *sprev; // [block][head][P][N] state entering each block (bf16 operand)
 };
 

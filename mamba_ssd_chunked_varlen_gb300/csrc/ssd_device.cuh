@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ssd_common.cuh"
 
@@ -34,6 +35,42 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// ---------------------------------------------------------------- block states
+// Block states cross the workspace as fp16, each group of 16 consecutive p
+// (one n) scaled by a power of two 2^k that puts the group's largest magnitude
+// in [2^14, 2^15): every value of the group down to 2^-28 of that maximum keeps
+// fp16's full 11-bit precision (relative rounding <= 2^-11), and no value
+// overflows, whatever the magnitude of the states.  k is stored beside them
+// as an int8 per group.
+__device__ __forceinline__ int state_group_exp(float maxabs)
+{
+    const int e = static_cast<int>((__float_as_uint(maxabs) >> 23) & 0xffu);
+    if (e == 0 || e == 255)
+        return 0;
+    return min(max(141 - e, -100), 100);
+}
+
+// 2^k for |k| <= 126.
+__device__ __forceinline__ float pow2i(int k)
+{
+    return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+}
+
+// A group of 16 state values rounded as they cross the workspace: fp16 after
+// scaling by the group's exponent, then back.
+__device__ __forceinline__ void round_state_group(float (&v)[16])
+{
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        m = fmaxf(m, fabsf(v[k]));
+    const int ke = state_group_exp(m);
+    const float sc = pow2i(ke), inv = pow2i(-ke);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        v[k] = __half2float(__float2half_rn(v[k] * sc)) * inv;
 }
 
 // Processed step of token t, head h: softplus(dt + dt_bias) (or dt + dt_bias).

@@ -593,6 +593,8 @@ bool use_state_walk(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb
     const WalkConfig c = state_walk_config(H, G, P, N, batch, sms);
     if (static_cast<int64_t>(batch) * (H / c.HB) * c.nT < sms)
         return false;
+    // the split design's block states (fp16) and entering states (bf16): 4 bytes
+    // per state element and block
     const int64_t state_bytes = (T + Qb - 1) / Qb * static_cast<int64_t>(H) * P * N * 4;
     return state_bytes > l2;
 }

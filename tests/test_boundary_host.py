@@ -44,17 +44,20 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     ws = binding.ssd_scan_varlen_workspace_size
     n1 = ws(4096, 1, 16, 64, 1, 256, 256)
-    # block states dominate: (ceil(T/128) + batch) blocks x H x P x N x (4 + 2) bytes
-    # (chunks longer than 128 tokens are processed as 128-token blocks)
-    assert n1 >= 33 * 16 * 64 * 256 * 6
-    assert n1 < 33 * 16 * 64 * 256 * 6 + 64 * 1024
+    # block states dominate: (ceil(T/128) + batch) blocks x H x P x N x (2 + 1/16 + 2)
+    # bytes (fp16 block states with an exponent byte per 16 of them, bf16 entering
+    # states; chunks longer than 128 tokens are processed as 128-token blocks)
+    per_block = 16 * 64 * 256 * 4 + 16 * 64 * 256 // 16
+    assert n1 >= 33 * per_block
+    assert n1 < 33 * per_block + 64 * 1024
     assert ws(4096, 1, 16, 64, 1, 256, 128) == n1
     assert ws(4096, 2, 16, 64, 1, 256, 256) > n1          # more sequences, more chunks
     # with several sequences, those of at most 12 tokens hold no block and at
     # most T / 13 sequences are longer: 256 one-token sequences need
     # ceil(256/128) + 19 = 21 blocks of scratch, not ceil(256/128) + 256
     nd = ws(256, 256, 64, 64, 1, 128, 256)
-    assert 21 * 64 * 64 * 128 * 6 <= nd < 21 * 64 * 64 * 128 * 6 + 64 * 1024
+    per_block_d = 64 * 64 * 128 * 4 + 64 * 64 * 128 // 16
+    assert 21 * per_block_d <= nd < 21 * per_block_d + 64 * 1024
     assert ws(0, 3, 4, 32, 1, 32, 64) > 0                 # empty sequences still need a table
     assert ws(512, 1, 4, 32, 1, 512, 64) == 0             # dstate > 256 (MAX_DSTATE)
     assert ws(512, 1, 4, 32, 1, 32, 100) == 0             # unsupported chunk size
