@@ -322,7 +322,9 @@ class L2Flush:
     def __init__(self, dev, write_only: bool = False):
         import torch
         self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-        self.r = None if write_only else torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32,
+        # fp32, so that the read is one reduction kernel (an int32 sum would
+        # first widen the buffer to int64)
+        self.r = None if write_only else torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32,
                                                     device=dev)
 
     def __call__(self, k: int):
