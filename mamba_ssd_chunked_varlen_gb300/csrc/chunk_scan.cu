@@ -163,8 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *s_part = reinterpret_cast<float *>(scratch + 40);   // 16 warp partials
     float *sD = reinterpret_cast<float *>(scratch + 56);       // D of the CTA's heads (<= 8)
 
-    const int blk = blockIdx.x;
-    const int h0 = blockIdx.y * HB;
+    const bool by_rows = blocks_on_y(p);
+    const int blk = by_rows ? blockIdx.y : blockIdx.x;
+    const int h0 = (by_rows ? blockIdx.x : blockIdx.y) * HB;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0)
         SSD_TRACE_EV(2, 0);
@@ -636,7 +637,7 @@ cudaError_t launch_chunk_scan(const ScanParams &p, const ChunkScanMaps &maps, cu
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.max_chunks, p.H / c.HB);
+    cfg.gridDim = blocks_on_y(p) ? dim3(p.H / c.HB, p.max_chunks) : dim3(p.max_chunks, p.H / c.HB);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = c.smem;
     cfg.stream = stream;

@@ -111,8 +111,9 @@ __global__ void __launch_bounds__(kThreads, kFinishSingle ? 1 : 2)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
     float *s_part = reinterpret_cast<float *>(scratch + 40);  // 16 warp partials
 
-    const int blk = blockIdx.x;
-    const int h0 = blockIdx.y * HB;
+    const bool by_rows = blocks_on_y(p);
+    const int blk = by_rows ? blockIdx.y : blockIdx.x;
+    const int h0 = (by_rows ? blockIdx.x : blockIdx.y) * HB;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // The per-call bookkeeping (block table, error word, slot checks) falls to
     // CTA (max_chunks - 1, 0): max_chunks bounds the number of blocks from
@@ -479,7 +480,7 @@ cudaError_t launch_chunk_state(const ScanParams &p, const ChunkStateMaps &maps,
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.max_chunks, p.H / c.HB);
+    cfg.gridDim = blocks_on_y(p) ? dim3(p.H / c.HB, p.max_chunks) : dim3(p.max_chunks, p.H / c.HB);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = c.smem;
     cfg.stream = stream;

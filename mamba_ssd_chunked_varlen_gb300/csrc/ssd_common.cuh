@@ -159,6 +159,18 @@ struct ScanParams {
     __nv_bfloat16 *sprev; // [block][head][P][N] state entering each block (bf16 operand)
 };
 
+// Grid of the two block kernels (chunk state and chunk scan): with the block
+// table (many-wave calls) it is (head groups, blocks), so that every block's
+// CTAs are dispatched before the empty block indices past the call's last
+// block (the host's bound counts a partial block for every sequence that may
+// be long) and a block's head groups run side by side; without it, (blocks,
+// head groups).  gridDim.y is at most 65535.
+__host__ __device__ inline bool blocks_on_y(const ScanParams &p)
+{
+    return p.table != nullptr && p.max_chunks <= 65535;
+}
+
+
 __device__ __forceinline__ void record_error(WsHeader *hdr, uint32_t flag)
 {
     atomicOr(&hdr->errors, flag);
