@@ -25,14 +25,17 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVec = 8;
-constexpr int kAhead = 8;  // blocks loaded ahead of use
 
-// at most 128 registers (the eight blocks' states, exponents and decays in
-// flight): one of these CTAs fits beside a chunk-state CTA on an SM while it
-// waits for it.  A persistent grid walks the (sequence, head, element range)
-// items of the sequences the chunk-state kernel listed as not short, so a
-// batch of short sequences costs no CTA here.
-__global__ void __launch_bounds__(kThreads, 2) state_passing_kernel(ScanParams p, int blocks_per_head)
+// kAhead blocks' states, exponents and decays are loaded before any of them
+// is used.  Long chains (sequences of many blocks) take 8 ahead at up to 128
+// registers, two CTAs per SM; calls of short sequences (a few blocks each, so
+// a deep prefetch mostly loads past their ends) take 4 ahead at up to 85
+// registers, three CTAs per SM, for more items in flight.  A persistent grid
+// walks the (sequence, head, element range) items of the sequences the
+// chunk-state kernel listed as not short, so a batch of short sequences costs
+// no CTA here.  Both forms compute the same values.
+template <int kAhead, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) state_passing_kernel(ScanParams p, int blocks_per_head)
 {
     if (threadIdx.x == 0)
         SSD_TRACE_EV(1, 0);
@@ -121,13 +124,15 @@ cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool 
     const int64_t PN = static_cast<int64_t>(p.P) * p.N;
     const int blocks_per_head = static_cast<int>((PN / kVec + kThreads - 1) / kThreads);
     cudaLaunchConfig_t cfg = {};
-    // one CTA per item up to two per SM (the register limit), each looping
-    // over items beyond that
+    // one CTA per item up to two (three) per SM, the register limit, each
+    // looping over items beyond that; sequences of at most 4 blocks on
+    // average take the shallow form
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool shallow = p.T <= 4 * static_cast<int64_t>(p.Q) * p.batch;
     const int64_t items = static_cast<int64_t>(blocks_per_head) * p.batch * p.H;
-    const int64_t cap = 2 * static_cast<int64_t>(sms);
+    const int64_t cap = (shallow ? 3 : 2) * static_cast<int64_t>(sms);
     cfg.gridDim = dim3(static_cast<unsigned>(items < cap ? items : cap));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
@@ -137,7 +142,9 @@ cudaError_t launch_state_passing(const ScanParams &p, cudaStream_t stream, bool 
     attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, state_passing_kernel, p, blocks_per_head);
+    if (shallow)
+        return cudaLaunchKernelEx(&cfg, state_passing_kernel<4, 3>, p, blocks_per_head);
+    return cudaLaunchKernelEx(&cfg, state_passing_kernel<8, 2>, p, blocks_per_head);
 }
 
 }  // namespace ssd
