@@ -355,7 +355,7 @@ SSD_API const char *ssd_status_string(ssd_status_t status);
  * ssd_scan_varlen_fused_walk says so), chunk scan when total_len > 0, the
  * short-sequence kernel when the call may hold short sequences, and a
  * block-map kernel for batches of more than 512 sequences or calls whose
- * chunk-scan grid would run more than two waves of one CTA per SM.  Used to
+ * chunk-scan grid would run more than four waves of one CTA per SM.  Used to
  * count launches when timing.  Reads the current device's SM count and L2
  * size. */
 SSD_API int32_t ssd_scan_varlen_num_launches(int64_t total_len, int32_t batch, int32_t nheads,

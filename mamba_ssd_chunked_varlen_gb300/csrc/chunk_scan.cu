@@ -600,8 +600,11 @@ bool use_block_table(int64_t T, int32_t batch, int H, int G, int P, int N, int Q
     const K3Config c = chunk_scan_config(H, G, P, N);
     if (c.HB == 0)
         return false;
+    // a per-CTA scan of query_start_loc costs one round trip per wave of the
+    // block kernels, the block-map kernel one launch in the chain: the table
+    // pays from about four waves of one CTA per SM on
     const int64_t ctas = max_chunks_bound(T, batch, Qb, short_len) * (H / c.HB);
-    return ctas > 2 * static_cast<int64_t>(sms);
+    return ctas > 4 * static_cast<int64_t>(sms);
 }
 
 K3Config chunk_scan_config(int H, int G, int P, int N)

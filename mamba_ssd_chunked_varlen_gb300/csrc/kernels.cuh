@@ -57,8 +57,8 @@ bool use_state_walk(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb
 
 // Whether a call maps its blocks once in the block-map kernel: batches of more
 // than kMapBatchMax sequences, and calls whose chunk-scan grid would run more
-// than two waves of one CTA per SM (a per-CTA block map costs each wave a
-// query_start_loc round trip).  Uses the current device's SM count (152 when
+// than four waves of one CTA per SM (a per-CTA block map costs each wave a
+// query_start_loc round trip, the block-map kernel one launch).  Uses the current device's SM count (152 when
 // no device answers).
 bool use_block_table(int64_t T, int32_t batch, int H, int G, int P, int N, int Qb, int short_len);
 

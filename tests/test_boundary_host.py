@@ -77,11 +77,13 @@ def test_launch_count(lib):
     assert n(0, 3) == 3         # empty sequences: no output kernel
     assert n(10, 0) == 0
     # a block-map kernel writes a block table for more than 512 sequences, or
-    # when the chunk-scan grid would run more than two waves (424 blocks x 4
+    # when the chunk-scan grid would run more than four waves (424 blocks x 4
     # head groups here); otherwise every CTA maps its own block
     assert n(5000, 512) == 5
     assert n(5000, 513) == 5
     assert n(5000, 30) == 4     # 70 blocks x 4 head groups: under two waves
+    assert n(15155, 8) == 4     # 127 blocks x 4 head groups: under four waves
+    assert n(40000, 30) == 5    # 343 blocks x 4 head groups: nine waves
     # long sequences with many heads whose block states exceed the L2: block
     # states and state passing in one fused kernel (and, at 260 blocks x 32
     # head groups, the block-map kernel)

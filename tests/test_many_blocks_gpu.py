@@ -1,6 +1,6 @@
 """Parity with the oracle, on every head, of calls that run many waves of the
 chunk-scan kernel through the block table (more (block, head group) CTAs than
-two per SM), for several dstate and B/C group shapes: dstate 128, 64, 96
+four per SM), for several dstate and B/C group shapes: dstate 128, 64, 96
 (padded to the 64-wide operand blocks) and 32, one to four B/C groups.
 Lengths mix sequences for the short-sequence kernel, exact multiples of 128
 tokens, ragged tails and long sequences; about half the sequences enter with
@@ -41,9 +41,9 @@ def _lens(rng, target):
 # (nheads, ngroups, dstate, target tokens)
 CASES = [
     pytest.param(8, 2, 128, 40_000, id="h8g2n128"),
-    pytest.param(4, 1, 64, 42_000, id="h4g1n64"),
+    pytest.param(4, 1, 64, 70_000, id="h4g1n64"),
     pytest.param(8, 4, 96, 24_000, id="h8g4n96"),
-    pytest.param(16, 2, 32, 12_000, id="h16g2n32"),
+    pytest.param(16, 2, 32, 20_000, id="h16g2n32"),
 ]
 
 
